@@ -1,0 +1,230 @@
+/*
+ * tfl.h - C ABI of a GB300 (sm_103a) bf16 forward for dense Llama-family GQA
+ * decoders of the Nanbeige4.3-33B shape (hidden 7168, 52 layers, 56 query and
+ * 8 KV heads of 128, FFN 22016, vocabulary 166,912, NeoX RoPE theta 1.2e8).
+ *
+ * What is computed (source: pull request #1415 "llama: Nanbeige4.3-33B on
+ * Metal, the bf16 release served as published", section "How"): HF
+ * modeling_llama in bf16, rounding to bf16 exactly at its rounding points:
+ *   residual      h = bf16(h + bf16(f(h)))
+ *   RMSNorm       bf16(w * bf16(x * rsqrt(mean(x^2) + eps)))
+ *   projections   fp32 sums rounded once to bf16 (weights read in place)
+ *   RoPE          bf16(bf16(x c) + bf16(rotate_half(x) s)), c/s = bf16 cos/sin
+ *                 of the fp32 angle pos * inv_freq, NeoX half-head pairs
+ *   attention     causal GQA (q head h reads KV head h / (n_q / n_kv)) over
+ *                 keys at absolute positions 0..pos, scale 1/sqrt(head_dim);
+ *                 scores, softmax and P.V in fp32, output rounded once
+ *   SwiGLU        bf16(bf16(silu(g)) * u)
+ *   head          final RMSNorm, lm_head (untied), greedy argmax with ties to
+ *                 the lower id (same pull request, teacher-forced misses reply)
+ *
+ * Memory ownership.  The caller owns every device buffer (weights, workspace,
+ * KV buffers, ids, logits) and keeps it alive while the library uses it; the
+ * library borrows device pointers and owns only small host metadata.  All
+ * tensors are bf16 unless stated, row-major, weights in HF [out][in] layout.
+ *
+ * Streams.  Every call that takes `stream` (a cudaStream_t, NULL = legacy
+ * default stream) only enqueues work on it and returns without synchronising,
+ * except tfl_status.  Host-side bookkeeping (KV lengths) advances at enqueue
+ * time.  A model or KV object must not be used from two host threads at once.
+ *
+ * Errors.  Every function returns TFL_OK (0) or a negative TFL_E_* code and
+ * throws nothing.  Arguments are validated on the host before anything is
+ * enqueued; on an error nothing is enqueued and no state changes.
+ * tfl_last_error() gives a message for the calling thread's last error.
+ */
+#ifndef TFL_H
+#define TFL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TFL_OK 0
+#define TFL_E_GEOMETRY (-1)  /* not a qualified geometry (message names it) */
+#define TFL_E_ARCH (-2)      /* the current device is not an sm_103 GPU */
+#define TFL_E_CAPACITY (-3)  /* a position would reach the KV capacity */
+#define TFL_E_ARG (-4)       /* bad pointer, size, count or alignment */
+#define TFL_E_CUDA (-5)      /* a CUDA runtime call failed */
+#define TFL_E_NONFINITE (-6) /* an argmax saw a NaN or +-Inf logit */
+#define TFL_E_WORKSPACE (-7) /* workspace or KV buffer too small */
+#define TFL_E_DEVICE (-8)    /* a kernel reported an internal error (bounded wait) */
+
+typedef struct tfl_model tfl_model;
+typedef struct tfl_kv tfl_kv;
+
+typedef struct {
+    int hidden;        /* H */
+    int layers;        /* L */
+    int n_q;           /* query heads */
+    int n_kv;          /* key/value heads */
+    int head_dim;      /* D, must be 128 */
+    int ffn;           /* F */
+    int vocab;         /* V */
+    double rope_theta; /* unscaled NeoX RoPE base */
+    float rms_eps;     /* RMSNorm epsilon */
+    int max_rows;      /* rows of one tfl_prefill_chunk, 1..2048 */
+    int max_decode_rows; /* total rows of one tfl_decode_step over all streams, 1..64 */
+    int max_context;   /* largest max_positions of any KV buffer used with the model */
+} tfl_config;
+
+/*
+ * Device pointers to the weights, bf16, HF layout.  Per-layer fields point to
+ * host arrays of `layers` device pointers (the arrays are copied at tfl_init).
+ * Every pointer must be 16-byte aligned.
+ *   embed [V][H], final_norm [H], lm_head [V][H] (untied: may not equal embed),
+ *   attn_norm [H], wq [n_q*D][H], wk [n_kv*D][H], wv [n_kv*D][H], wo [H][n_q*D],
+ *   ffn_norm [H], wg [F][H], wu [F][H], wd [H][F].
+ */
+typedef struct {
+    const void *embed, *final_norm, *lm_head;
+    const void *const *attn_norm, *const *wq, *const *wk, *const *wv, *const *wo;
+    const void *const *ffn_norm, *const *wg, *const *wu, *const *wd;
+} tfl_weights;
+
+/* ---- setup ---------------------------------------------------------------- */
+
+/*
+ * Host-only geometry check (no GPU needed).  Qualified geometries: the 33B
+ * shape above with 1..52 layers (a truncated stack of the same model), and the
+ * tiny test model (hidden 1024, 8 q / 1 KV head of 128, FFN 2816, vocab 4096,
+ * 1..2 layers).  Also refuses head_dim != 128, non-positive sizes, and
+ * max_rows / max_decode_rows / max_context outside their ranges.  This mirrors
+ * the qualification gate of pull request #1415 (reply "Admission"): other
+ * geometries are refused by name.  On refusal, writes a message into msg
+ * (if msg_len > 0) and returns TFL_E_GEOMETRY or TFL_E_ARG.
+ */
+int tfl_qualify(const tfl_config* cfg, char* msg, size_t msg_len);
+
+/* Bytes of device workspace tfl_init needs for cfg (0 if cfg is not qualified). */
+size_t tfl_workspace_bytes(const tfl_config* cfg);
+
+/*
+ * Creates a model.  Checks cfg (tfl_qualify), that the current device is
+ * sm_103 (TFL_E_ARCH otherwise, named in the message), pointer alignment and
+ * ws_bytes >= tfl_workspace_bytes(cfg).  Builds the bf16 RoPE cos/sin table
+ * for max_context positions on the host and uploads it into the workspace
+ * (synchronously, on the legacy default stream).  The workspace (16-byte
+ * aligned device memory) is owned by the caller and used exclusively by this
+ * model until tfl_free.
+ */
+int tfl_init(const tfl_config* cfg, const tfl_weights* weights, void* workspace, size_t ws_bytes,
+             tfl_model** out);
+void tfl_free(tfl_model* model);
+
+/* Thread-local message for the last error returned to this thread ("" if none). */
+const char* tfl_last_error(void);
+const char* tfl_error_string(int code);
+
+/* ---- KV cache ---------------------------------------------------------------- */
+
+/*
+ * Position-major paged bf16 cache.  A buffer of tfl_kv_bytes(cfg, P) bytes holds
+ * a page table (int32 per page, logical page -> physical page, identity after
+ * tfl_kv_alloc) followed by pages of TFL_KV_PAGE positions; within a page the
+ * layout is [position][kv head][D] for keys and, separately, for values:
+ *   K(layer, pos) at pages + (((layer*2 + 0)*n_pages + table[pos/PAGE])*PAGE + pos%PAGE)*n_kv*D
+ *   V(layer, pos) at pages + (((layer*2 + 1)*n_pages + table[pos/PAGE])*PAGE + pos%PAGE)*n_kv*D
+ * i.e. layers * 2 * n_kv * D * 2 bytes per position (212,992 B for the 33B
+ * shape: the 208 KiB/token of the EXL3 model card's "Which rung" section).
+ * Keys are stored after RoPE.
+ */
+#define TFL_KV_PAGE 128
+size_t tfl_kv_bytes(const tfl_config* cfg, int max_positions);
+
+/*
+ * Creates a KV object over dev_buf (16-byte aligned, >= tfl_kv_bytes bytes,
+ * owned by the caller).  1 <= max_positions <= cfg.max_context.  Writes the
+ * identity page table (synchronously).  The length starts at 0.
+ */
+int tfl_kv_alloc(tfl_model* model, int max_positions, void* dev_buf, size_t bytes, tfl_kv** out);
+void tfl_kv_free(tfl_kv* kv);
+
+/*
+ * Sets the length (number of valid positions) to keep, 0 <= keep <=
+ * max_positions.  keep < length truncates to a kept prefix (resume: the next
+ * call continues at position keep).  keep > length declares positions
+ * [length, keep) valid; their contents must have been written by earlier calls
+ * or by tfl_kv_write.  Host-only; enqueues nothing.
+ */
+int tfl_kv_reset(tfl_kv* kv, int keep);
+int tfl_kv_length(const tfl_kv* kv);
+int tfl_kv_capacity(const tfl_kv* kv);
+
+/*
+ * Copies n positions [pos0, pos0+n) of one layer between the cache and dense
+ * device tensors k, v of shape [n][n_kv][D] (keys after RoPE).  write: dense ->
+ * cache; read: cache -> dense.  Does not change the length.  Bounds: 0 <= layer
+ * < layers, 0 <= pos0, pos0 + n <= max_positions.
+ */
+int tfl_kv_write(tfl_model* model, tfl_kv* kv, int layer, int pos0, int n, const void* k, const void* v,
+                 void* stream);
+int tfl_kv_read(tfl_model* model, const tfl_kv* kv, int layer, int pos0, int n, void* k, void* v,
+                void* stream);
+
+/* ---- forward ------------------------------------------------------------------ */
+
+/*
+ * One decode step over n_streams streams (1..16) sharing the weight pass.
+ * Stream s contributes rows_per_stream[s] (host array, 1..16) consecutive rows
+ * of ids (device int32 [sum rows], stream-major), at positions length(s) ..
+ * length(s) + rows - 1; a multi-row group is a causal window (each row sees
+ * the earlier rows of the same stream).  Writes logits (device bf16 [sum
+ * rows][V]) and appends the rows' keys and values; length(s) += rows.
+ * The same kvs object may not appear twice.  TFL_E_CAPACITY if a stream would
+ * pass its max_positions (nothing is enqueued then).  Results for each row are
+ * bit-identical whatever the other rows and streams of the call are
+ * (one-row steps == windows, solo == batched).
+ */
+int tfl_decode_step(tfl_model* model, tfl_kv* const* kvs, int n_streams, const int32_t* ids,
+                    const int* rows_per_stream, void* logits, void* stream);
+
+/*
+ * Prompt chunk of n_rows (1..max_rows) ids (device int32) for one stream, at
+ * positions length .. length + n_rows - 1 (causal over the cache and the
+ * chunk).  logits: NULL for none; else device bf16 [1][V] for the last row
+ * (all_rows == 0) or [n_rows][V] (all_rows != 0).  length += n_rows.
+ * The row results do not depend on where chunk boundaries fall (a prompt
+ * resumed from a kept prefix equals the same prompt prefilled fresh).
+ */
+int tfl_prefill_chunk(tfl_model* model, tfl_kv* kv, const int32_t* ids, int n_rows, void* logits,
+                      int all_rows, void* stream);
+
+/*
+ * Greedy ids (device int32 [n_rows]) from logits (device bf16 [n_rows][V]),
+ * ties to the lowest id.  A row holding NaN or +-Inf gets id -1 and raises the
+ * model's device status word, read by tfl_status.
+ */
+int tfl_argmax(tfl_model* model, const void* logits, int n_rows, int32_t* ids, void* stream);
+
+/*
+ * Synchronises `stream`, reads and clears the device status word: returns
+ * TFL_OK, TFL_E_NONFINITE (an argmax saw a non-finite logit) or TFL_E_DEVICE
+ * (a kernel gave up a bounded wait), or TFL_E_CUDA if the stream had failed.
+ */
+int tfl_status(tfl_model* model, void* stream);
+
+/* ---- component entry points (the same kernels, for per-layer checks) ------- */
+
+/*
+ * The decoder layers only: like tfl_decode_step / tfl_prefill_chunk but the
+ * rows are given as residual-stream rows h_in (device bf16 [rows][H], the
+ * embedding output) and the result is the residual stream after the last
+ * layer, h_out (device bf16 [rows][H]), before the final norm.  decode: the
+ * decode kernels (n_streams, rows_per_stream as tfl_decode_step); prefill: the
+ * prompt-chunk kernels for one stream.  KV lengths advance as in the full calls.
+ */
+int tfl_decode_hidden(tfl_model* model, tfl_kv* const* kvs, int n_streams, const int* rows_per_stream,
+                      const void* h_in, void* h_out, void* stream);
+int tfl_prefill_hidden(tfl_model* model, tfl_kv* kv, const void* h_in, int n_rows, void* h_out, void* stream);
+
+/* Final RMSNorm + lm_head over rows of h (device bf16 [rows][H]) -> logits [rows][V]. */
+int tfl_head(tfl_model* model, const void* h, int rows, void* logits, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TFL_H */
