@@ -1,0 +1,368 @@
+#!/usr/bin/env python
+"""Decode benchmark of the 33B-shaped bf16 GQA decoder on GB300.
+
+Workload: the full 52-layer Nanbeige4.3-33B-shaped model with random-init bf16
+weights (seed 21, ~61.7 GiB), an 8,192-token prompt of uniform-random ids (seed
+22) prefilled in 2,048-row chunks, then batch-1 greedy decode: one step = one
+decode row through all 52 layers + lm_head + argmax, the next id staying on the
+device.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tfl|reference]
+
+--impl reference times the CPU oracle (the slow float64 reference) on the host
+cores for the same metric.  With N > 1 (torchrun) every rank runs an independent
+replica (the path has no data-parallel exchange: replicas only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gqa_decoder_forward_gb300 import synth  # noqa: E402
+
+METRIC = "33B bf16 decode tok/s @1 stream + HBM GB/s vs peak; prefill tok/s"
+SHAPE = synth.NANBEIGE_33B
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=64)
+    p.add_argument("--warmup", type=int, default=8)
+    p.add_argument("--impl", choices=["tfl", "reference"], default="tfl")
+    p.add_argument("--context", type=int, default=8192)
+    p.add_argument("--layers", type=int, default=SHAPE.layers)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ---- environment ---------------------------------------------------------------------
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "tfl" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- algorithmic bytes --------------------------------------------------------------
+
+def layer_weight_bytes(m) -> int:
+    return sum(2 * int(torch.tensor(s).prod()) for s in synth.layer_tensor_shapes(m).values())
+
+
+def step_bytes(m, ctx: int) -> int:
+    """Bytes a batch-1 decode step must move: every weight but the embedding
+    table (one embedding row), plus the keys and values of ctx positions."""
+    w = m.layers * layer_weight_bytes(m) + 2 * m.hidden + m.vocab * m.hidden * 2 + m.hidden * 2
+    kv = m.layers * 2 * m.n_kv * m.head_dim * 2 * ctx
+    return w + kv
+
+
+# ---- oracle (CPU) timing ----------------------------------------------------------------
+
+def oracle_sample(context: int, min_seconds: float = 10.0):
+    """Times the oracle on one 33B-shaped layer's decode step (one row at position
+    `context` over a seeded cache) and on the lm_head of one row; returns
+    (seconds per token for the 52-layer model, threads, description)."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    one = SHAPE.with_layers(1)
+    w = {k: [synth.layer_weight(one, 21, 0, k, dev)] for k in synth.LAYER_KEYS}
+    hw = {k: [synth.bits(w[k][0])] for k in synth.LAYER_KEYS}
+    hw["embed"] = np.zeros(8, np.uint16)
+    hw["final_norm"] = synth.bits(synth.global_weight(one, 21, "final_norm", dev))
+    hw["lm_head"] = synth.bits(synth.global_weight(one, 21, "lm_head", dev))
+    del w
+    c = oracle.Config(one.hidden, 1, one.n_q, one.n_kv, one.head_dim, one.ffn, one.vocab, one.rope_theta,
+                      one.rms_eps)
+    om = oracle.Model(c, hw, context + 1)
+    K, V = synth.kv_contents(one, 12, 0, context, dev)
+    om.K[0, :context] = synth.bits(K)
+    om.V[0, :context] = synth.bits(V)
+    h = synth.bits(synth.hidden_rows(one, 13, 1, dev))
+    pos = np.array([context], np.int32)
+    om.layer(0, h, pos)  # warm
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        out = om.layer(0, h, pos)
+        reps += 1
+        if time.perf_counter() - t0 >= min_seconds * 0.8:
+            break
+    t_layer = (time.perf_counter() - t0) / reps
+    t1 = time.perf_counter()
+    om.head(out)
+    t_head = time.perf_counter() - t1
+    per_token = SHAPE.layers * t_layer + t_head
+    desc = (f"oracle: {reps} reps of one 33B-shaped layer decode step (1 row at position {context}, seeded KV) "
+            f"= {t_layer * 1e3:.1f} ms, x{SHAPE.layers} layers + one lm_head row {t_head * 1e3:.0f} ms")
+    return per_token, oracle.get_threads(), desc, t_layer, t_head
+
+
+# ---- the two arms ---------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    ctx = args.context
+    per_tok, cores, desc, t_layer, t_head = oracle_sample(ctx, min_seconds=3.0)
+    # each timed step: one layer of the oracle (a bounded sample of the 52-layer step)
+    import numpy as np  # noqa: F401
+    value = 1.0 / per_tok
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_tok * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"Nanbeige4.3-33B-shaped decode, 1 stream, context {ctx}", "context": ctx,
+                   "rows": 1, "layers": SHAPE.layers},
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_tfl(args, world, rank, local):
+    from gqa_decoder_forward_gb300 import build, tfl
+    if rank == 0 or world == 1:
+        build.build()
+    barrier(world)
+    tfl.lib()
+    shape = SHAPE.with_layers(args.layers)
+    ctx = args.context
+    extra = args.warmup + args.steps + 16 + 16 + 8
+    max_ctx = ctx + extra
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    weights = synth.model_weights(shape, 21, dev)
+    torch.cuda.synchronize()
+    model = tfl.Model(shape, weights, max_rows=2048, max_decode_rows=16, max_context=max_ctx)
+    kv = model.kv(max_ctx)
+    ids = synth.uniform_ids(22, ctx, shape.vocab, dev)
+    st = torch.cuda.current_stream()
+
+    # prefill (the prompt-chunk path), timed once
+    logits = torch.empty((1, shape.vocab), dtype=torch.bfloat16, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for c in range(0, ctx, 2048):
+        model.prefill_chunk(kv, ids[c:c + 2048].contiguous(), logits if c + 2048 >= ctx else None)
+    e1.record(st)
+    torch.cuda.synchronize()
+    prefill_s = e0.elapsed_time(e1) / 1e3
+    nxt = torch.empty(1, dtype=torch.int32, device=dev)
+    model.argmax(logits, nxt)
+
+    def step():
+        model.decode_step([kv], nxt, [1], logits)
+        model.argmax(logits, nxt)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ctx0 = kv.length
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(st)
+        for _ in range(args.steps):
+            step()
+        t1.record(st)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world)
+    status = model.status()
+    mean_ctx = ctx0 + (args.steps - 1) / 2.0
+
+    # per-kernel times (profiled pass: events around every launch)
+    prof_steps = min(16, args.steps)
+    tfl.tfl_profile(model, True)
+    for _ in range(prof_steps):
+        step()
+    prof = tfl.tfl_profile_read(model)
+    tfl.tfl_profile(model, False)
+    launches_per_step = sum(n for _, n in prof.values()) / prof_steps
+
+    # end to end through the C ABI with host buffers: id in (pinned, H2D), id out (D2H)
+    e2e_steps = min(16, args.steps)
+    host_in = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    host_out = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    host_in.copy_(nxt.cpu())
+    dev_in = torch.empty(1, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        dev_in.copy_(host_in, non_blocking=True)
+        model.decode_step([kv], dev_in, [1], logits)
+        model.argmax(logits, nxt)
+        host_out.copy_(nxt, non_blocking=True)
+        st.synchronize()
+        host_in.copy_(host_out)
+    e2e_s = (time.perf_counter() - w0) / e2e_steps
+    e2e_s = max_over_ranks(e2e_s, world)
+
+    peak, peak_kind = measured_peaks()
+    step_b = step_bytes(shape, int(round(mean_ctx)))
+    step_gbs = step_b / (ms / 1e3) / 1e9
+    dom = max(prof.items(), key=lambda kv_: kv_[1][0])
+    dom_name, (dom_ms, dom_n) = dom
+    H, F = shape.hidden, shape.ffn
+    dom_bytes = {
+        "matvec_gate_up_swiglu": 2 * F * H * 2 + H * 2 + F * 2,
+        "matvec_down_residual": H * F * 2 + F * 2 + 2 * H * 2,
+        "matvec_qkv_rope": (shape.n_q + 2 * shape.n_kv) * 128 * H * 2 + H * 2,
+        "matvec_o_residual": H * H * 2 + 3 * H * 2,
+        "matvec_lm_head": shape.vocab * H * 2 + H * 2 + shape.vocab * 2,
+    }.get(dom_name)
+    roof = None
+    if dom_bytes is not None:
+        ach = dom_bytes / (dom_ms / dom_n / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom_name, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                "bytes_per_launch": dom_bytes, "us_per_launch": round(dom_ms / dom_n * 1e3, 2)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        per_tok, cores, desc, _, _ = oracle_sample(ctx, min_seconds=10.0)
+        cpu = {"value": 1.0 / per_tok, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+    value = world * 1e3 / ms
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights, uniform-random ids)",
+        "config": {"workload": f"Nanbeige4.3-33B-shaped decode, {args.layers} layers, 1 stream x 1 row, "
+                               f"context {ctx} (+{args.warmup} warm-up)",
+                   "context_mean": mean_ctx, "rows": 1, "streams": 1, "layers": args.layers,
+                   "l2": "inputs larger than L2 (61.7 GiB of weights streamed per step)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "step_hbm": {"bytes": step_b, "achieved_gbs": round(step_gbs, 1), "peak_gbs": peak,
+                     "frac": round(step_gbs / peak, 4), "peak_kind": peak_kind},
+        "roofline": roof,
+        "prefill": {"tokens": ctx, "seconds": round(prefill_s, 4), "tok_s": round(ctx / prefill_s, 1),
+                    "path": "prompt chunks of 2,048 rows"},
+        "kernels": {k: {"ms_per_step": round(v[0] / prof_steps, 4), "launches_per_step": v[1] / prof_steps}
+                    for k, v in prof.items() if v[1]},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "e2e": {"value": round(world / e2e_s, 3), "unit": "tok/s", "h2d_bytes_per_step": 4,
+                "d2h_bytes_per_step": 4},
+        "clocks": clk.summary(),
+        "status": status,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_tfl(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,114 @@
+// Internal declarations shared by the sm_103a kernels and the host orchestrator.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace tfl {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int kHeadDim = 128;      // D: the only head size the library serves
+constexpr int kPage = 128;         // KV positions per page (== decode key block)
+constexpr int kMaxStreams = 16;    // streams in one decode step
+constexpr int kMaxDecodeRows = 64; // rows in one decode step, over all streams
+constexpr int kMaxChunkRows = 2048;
+
+// Device status word bits (read and cleared by tfl_status).
+constexpr int kStatusNonFinite = 1;  // an argmax row held NaN / +-Inf
+constexpr int kStatusBadToken = 2;   // a token id outside [0, vocab)
+constexpr int kStatusDevice = 4;     // a bounded wait gave up
+
+// One stream's paged cache: K(layer,pos) / V(layer,pos) rows of n_kv*D bf16.
+struct KvView {
+    bf16* pages;       // first page
+    const int* table;  // logical page -> physical page
+    int n_pages;
+    int pad_;
+};
+
+// Rows of one call, grouped by stream: rows [row_start[s], row_start[s+1])
+// belong to stream s and sit at positions pos0[s], pos0[s]+1, ...
+struct RowMap {
+    int n_streams;
+    int n_rows;
+    int row_start[kMaxStreams + 1];
+    int pos0[kMaxStreams];
+    KvView kv[kMaxStreams];
+};
+
+__device__ __forceinline__ int row_stream(const RowMap& m, int r) {
+    int s = 0;
+    while (s + 1 < m.n_streams && r >= m.row_start[s + 1]) ++s;
+    return s;
+}
+
+__device__ __forceinline__ bf16* kv_row(const KvView& v, int layer, int kind, int pos, int n_kv) {
+    int page = __ldg(v.table + pos / kPage);
+    size_t idx = (((size_t)(layer * 2 + kind) * v.n_pages + page) * kPage + pos % kPage) * (size_t)n_kv * kHeadDim;
+    return v.pages + idx;
+}
+
+__device__ __forceinline__ float bf(bf16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ bf16 rn(float x) { return __float2bfloat16_rn(x); }
+__device__ __forceinline__ float rbf(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// Programmatic dependent launch: wait for the grids this one depends on (no-op
+// when launched without the attribute), and allow dependents to start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---- kernel launchers (each returns the cudaError_t of its launch) ----------
+
+// Epilogues of the decode matvec (fused into the projection).
+enum MatvecMode { MV_STORE = 0, MV_RESIDUAL = 1, MV_SWIGLU = 2, MV_QKV_ROPE = 3 };
+
+struct MatvecArgs {
+    int mode;
+    int K;                 // reduction length (multiple of 256)
+    int n_rows;            // activation rows, 1..64
+    const bf16* x;         // [n_rows][K]
+    // weights: STORE/RESIDUAL use w0 ([N][K]); SWIGLU w0 = gate, w1 = up ([F][K]);
+    // QKV_ROPE w0 = Wq, w1 = Wk, w2 = Wv.
+    const bf16* w0;
+    const bf16* w1;
+    const bf16* w2;
+    int n_out;             // STORE/RESIDUAL: N; SWIGLU: F; QKV: unused
+    int n_q, n_kv;         // QKV heads
+    bf16* y;               // STORE: [n_rows][ldy]; SWIGLU: [n_rows][F]; QKV: q out [n_rows][n_q*D]
+    long ldy;
+    bf16* h;               // RESIDUAL: [n_rows][N] updated in place
+    const bf16* cos_t;     // QKV: [positions][64]
+    const bf16* sin_t;
+    int layer;             // QKV: cache layer
+    RowMap rows;           // QKV: positions and caches of the rows
+};
+cudaError_t launch_matvec(const MatvecArgs& a, cudaStream_t st, bool pdl);
+
+cudaError_t launch_embed_rmsnorm(const int32_t* ids, const bf16* embed, int vocab, const bf16* w, float eps,
+                                 int n_rows, int H, bf16* h, bf16* xn, int* status, cudaStream_t st, bool pdl);
+cudaError_t launch_rmsnorm(const bf16* x, const bf16* w, float eps, int n_rows, int H, bf16* out,
+                           cudaStream_t st, bool pdl);
+
+struct AttnDecodeArgs {
+    const bf16* q;        // [n_rows][n_q*D] rotated
+    bf16* out;            // [n_rows][n_q*D]
+    float* pm;            // [n_rows][n_q][max_blocks]
+    float* pl;
+    float* po;            // [n_rows][n_q][max_blocks][D]
+    int max_blocks;
+    int n_q, n_kv, layer;
+    RowMap rows;
+};
+cudaError_t init_attn_decode();
+cudaError_t launch_attn_block(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
+cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
+
+cudaError_t launch_argmax(const bf16* logits, int n_rows, int V, int32_t* ids, int* status, cudaStream_t st,
+                          bool pdl);
+
+cudaError_t launch_kv_copy(bf16* cache_pages, const int* table, int n_pages, int n_kv, int layer, int pos0, int n,
+                           bf16* k, bf16* v, bool to_cache, cudaStream_t st);
+
+}  // namespace tfl

@@ -71,8 +71,9 @@ def _key(seed: int, tensor_id: int) -> int:
 
 
 def _words(key: int, idx: torch.Tensor, lane: int) -> torch.Tensor:
-    # two mixing rounds over (index, lane) keyed by (seed, tensor id)
-    return _mix32(_mix32((idx * 4 + lane) & _M32) ^ key)
+    # mixing rounds over (low index word ^ key), then (high index word, lane)
+    h = _mix32((idx & _M32) ^ key)
+    return _mix32(h ^ (((idx >> 32) * 0x632BE5AB + lane * 0x9E3779B9 + 0x7F4A7C15) & _M32))
 
 
 def _normal_f32(key: int, start: int, n: int, device) -> torch.Tensor:
@@ -89,7 +90,6 @@ def normal_bf16(seed: int, tensor_id: int, shape, std: float, device="cpu", mean
     numel = 1
     for s in shape:
         numel *= s
-    assert numel < (1 << 30), "index space of one tensor is 2^30 elements"
     key = _key(seed, tensor_id)
     out = torch.empty(numel, dtype=torch.bfloat16, device=device)
     scale = torch.tensor(std / _IH_SIGMA, dtype=torch.float32, device=device)

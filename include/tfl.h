@@ -99,6 +99,17 @@ typedef struct {
  */
 int tfl_qualify(const tfl_config* cfg, char* msg, size_t msg_len);
 
+/*
+ * The bf16 RoPE table tfl_init uploads, computed on the host (no GPU needed):
+ * for position p < n_pos and pair i < 64 (head_dim 128),
+ *   inv_freq[i] = fl32(1 / fl32(theta^(2i/128))),  a = fl32(p * inv_freq[i]),
+ *   cos_out[p*64 + i] = bf16(cos(a)),  sin_out[p*64 + i] = bf16(sin(a))
+ * with cos/sin evaluated in double and rounded once to bf16 (nearest, ties to
+ * even).  "bf16 cos and sin of the fp32 angle": pull request #1415, "How".
+ * Outputs are bf16 bit patterns in host arrays of n_pos*64 entries.
+ */
+void tfl_rope_table(double theta, int n_pos, uint16_t* cos_out, uint16_t* sin_out);
+
 /* Bytes of device workspace tfl_init needs for cfg (0 if cfg is not qualified). */
 size_t tfl_workspace_bytes(const tfl_config* cfg);
 
@@ -223,6 +234,57 @@ int tfl_prefill_hidden(tfl_model* model, tfl_kv* kv, const void* h_in, int n_row
 
 /* Final RMSNorm + lm_head over rows of h (device bf16 [rows][H]) -> logits [rows][V]. */
 int tfl_head(tfl_model* model, const void* h, int rows, void* logits, void* stream);
+
+/*
+ * One operation of the decode path, run by the same kernel a decode step uses,
+ * on caller-given device inputs (so each kernel can be checked alone against
+ * a reference fed the same bf16 inputs).  rows: 1..max_decode_rows, all of one
+ * stream at positions pos0 .. pos0+rows-1 (kv and pos0 are used by QKV_ROPE
+ * and ATTENTION only; other ops take kv = NULL).  Does not change KV lengths.
+ *   TFL_OP_ATTN_NORM     in h [rows][H]           -> out bf16 RMSNorm with attn_norm[layer]
+ *   TFL_OP_QKV_ROPE      in xn [rows][H]          -> out rotated q [rows][n_q*D]; rotated k and
+ *                        v of the rows written into kv (layer) at their positions
+ *   TFL_OP_ATTENTION     in rotated q [rows][n_q*D] -> out [rows][n_q*D]; row i attends
+ *                        keys 0..pos0+i of kv (layer), which must already hold them
+ *   TFL_OP_O_RESIDUAL    in attention out [rows][n_q*D]; out h [rows][H] updated in place:
+ *                        h = bf16(h + bf16(Wo[layer] . in))
+ *   TFL_OP_FFN_NORM      in h -> out RMSNorm with ffn_norm[layer]
+ *   TFL_OP_GATE_UP       in xn [rows][H] -> out bf16(bf16(silu(Wg.xn)) * Wu.xn) [rows][F]
+ *   TFL_OP_DOWN_RESIDUAL in act [rows][F]; out h updated: h = bf16(h + bf16(Wd[layer] . in))
+ *   TFL_OP_FINAL_NORM    in h -> out RMSNorm with final_norm (layer ignored)
+ *   TFL_OP_LM_HEAD       in xn [rows][H] -> out logits [rows][V] (layer ignored)
+ * Buffers are 16-byte aligned; in and out must not overlap.
+ */
+#define TFL_OP_ATTN_NORM 0
+#define TFL_OP_QKV_ROPE 1
+#define TFL_OP_ATTENTION 2
+#define TFL_OP_O_RESIDUAL 3
+#define TFL_OP_FFN_NORM 4
+#define TFL_OP_GATE_UP 5
+#define TFL_OP_DOWN_RESIDUAL 6
+#define TFL_OP_FINAL_NORM 7
+#define TFL_OP_LM_HEAD 8
+int tfl_layer_op(tfl_model* model, int op, int layer, tfl_kv* kv, int pos0, int rows, const void* in, void* out,
+                 void* stream);
+
+/* ---- per-kernel timing ------------------------------------------------------------- */
+
+/*
+ * While enabled, every kernel launch of the model is bracketed by two CUDA
+ * events recorded on the launch stream (this also serialises kernels that
+ * would otherwise overlap through programmatic dependent launch, so profiled
+ * steps run slightly slower than unprofiled ones).  Off after tfl_init.
+ */
+int tfl_profile(tfl_model* model, int enable);
+
+/*
+ * Synchronises the device and returns, per kernel family k < n_kinds, the
+ * summed elapsed milliseconds ms[k] and the number of launches[k] recorded
+ * since the last read (host arrays of n_kinds entries); then forgets them.
+ * Family names: tfl_profile_kind(k) (NULL past the last family).
+ */
+int tfl_profile_read(tfl_model* model, int n_kinds, double* ms, long* launches);
+const char* tfl_profile_kind(int kind);
 
 #ifdef __cplusplus
 }

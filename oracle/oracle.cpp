@@ -141,17 +141,20 @@ void orc_rmsnorm(const uint16_t* x, const uint16_t* w, int rows, int H, double e
 }
 
 // out[r][n] = bf16(sum_k W[n][k] * x[r][k]); W is [N][K] row-major (HF [out, in]).
+// Each sum runs over k in increasing order in double.
 void orc_linear(const uint16_t* W, int N, int K, const uint16_t* x, int rows, uint16_t* out) {
     std::vector<double> xd((size_t)rows * K);
     for (size_t i = 0; i < xd.size(); ++i) xd[i] = bf16_val(x[i]);
     parallel_for(N, [&](long n) {
         const uint16_t* wn = W + n * (long)K;
-        std::vector<double> acc(rows, 0.0);
-        for (int k = 0; k < K; ++k) {
-            double wv = bf16_val(wn[k]);
-            for (int r = 0; r < rows; ++r) acc[r] += wv * xd[(size_t)r * K + k];
+        std::vector<double> wd(K);
+        for (int k = 0; k < K; ++k) wd[k] = bf16_val(wn[k]);
+        for (int r = 0; r < rows; ++r) {
+            const double* xr = xd.data() + (size_t)r * K;
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) acc += wd[k] * xr[k];
+            out[(long)r * N + n] = bf16_round(acc);
         }
-        for (int r = 0; r < rows; ++r) out[(long)r * N + n] = bf16_round(acc[r]);
     });
 }
 
