@@ -43,6 +43,12 @@ def parse():
     p.add_argument("--context", type=int, default=8192)
     p.add_argument("--layers", type=int, default=SHAPE.layers)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--kv", choices=["prefill", "seeded"], default="prefill",
+                   help="build the context by prefilling the prompt, or write seeded KV contents")
+    p.add_argument("--op", default=None,
+                   help="time one decode op (qkv_rope, attention, o_residual, gate_up, down_residual, attn_norm) "
+                        "on a one-layer 33B-shaped model instead of the full step")
+    p.add_argument("--rows", type=int, default=1, help="rows per step for --op")
     return p.parse_args()
 
 
@@ -232,22 +238,30 @@ def run_tfl(args, world, rank, local):
 
     weights = synth.model_weights(shape, 21, dev)
     torch.cuda.synchronize()
-    model = tfl.Model(shape, weights, max_rows=2048, max_decode_rows=16, max_context=max_ctx)
+    model = tfl.Model(shape, weights, max_rows=2048, max_decode_rows=64, max_context=max_ctx)
     kv = model.kv(max_ctx)
     ids = synth.uniform_ids(22, ctx, shape.vocab, dev)
     st = torch.cuda.current_stream()
-
-    # prefill (the prompt-chunk path), timed once
     logits = torch.empty((1, shape.vocab), dtype=torch.bfloat16, device=dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for c in range(0, ctx, 2048):
-        model.prefill_chunk(kv, ids[c:c + 2048].contiguous(), logits if c + 2048 >= ctx else None)
-    e1.record(st)
-    torch.cuda.synchronize()
-    prefill_s = e0.elapsed_time(e1) / 1e3
     nxt = torch.empty(1, dtype=torch.int32, device=dev)
-    model.argmax(logits, nxt)
+
+    prefill_s = None
+    if args.kv == "prefill":
+        # prefill (the prompt-chunk path), timed once
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for c in range(0, ctx, 2048):
+            model.prefill_chunk(kv, ids[c:c + 2048].contiguous(), logits if c + 2048 >= ctx else None)
+        e1.record(st)
+        torch.cuda.synchronize()
+        prefill_s = e0.elapsed_time(e1) / 1e3
+        model.argmax(logits, nxt)
+    else:
+        for l in range(shape.layers):
+            K, V = synth.kv_contents(shape, 22, l, ctx, dev)
+            kv.write(l, 0, K, V)
+        kv.reset(ctx)
+        nxt.copy_(ids[-1:])
 
     def step():
         model.decode_step([kv], nxt, [1], logits)
@@ -337,8 +351,9 @@ def run_tfl(args, world, rank, local):
         "step_hbm": {"bytes": step_b, "achieved_gbs": round(step_gbs, 1), "peak_gbs": peak,
                      "frac": round(step_gbs / peak, 4), "peak_kind": peak_kind},
         "roofline": roof,
-        "prefill": {"tokens": ctx, "seconds": round(prefill_s, 4), "tok_s": round(ctx / prefill_s, 1),
-                    "path": "prompt chunks of 2,048 rows"},
+        "prefill": ({"tokens": ctx, "seconds": round(prefill_s, 4), "tok_s": round(ctx / prefill_s, 1),
+                     "path": "prompt chunks of 2,048 rows"} if prefill_s else None),
+        "kv": args.kv,
         "kernels": {k: {"ms_per_step": round(v[0] / prof_steps, 4), "launches_per_step": v[1] / prof_steps}
                     for k, v in prof.items() if v[1]},
         "gpu_launches": int(round(launches_per_step * args.steps)),
@@ -352,8 +367,50 @@ def run_tfl(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_op(args):
+    """Times one decode op on a one-layer 33B-shaped model (a few GB on the device):
+    the small case the kernel profiles are taken on."""
+    from gqa_decoder_forward_gb300 import build, tfl
+    build.build()
+    one = SHAPE.with_layers(1)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = {k: [synth.layer_weight(one, 21, 0, k, dev)] for k in synth.LAYER_KEYS}
+    # the op entry points never read the embedding table or lm_head: small stand-ins
+    w["embed"] = torch.zeros(64, dtype=torch.bfloat16, device=dev)
+    w["final_norm"] = torch.ones(one.hidden, dtype=torch.bfloat16, device=dev)
+    w["lm_head"] = torch.zeros(64, dtype=torch.bfloat16, device=dev)
+    R, ctx = args.rows, args.context
+    m = tfl.Model(one, w, max_rows=64, max_decode_rows=64, max_context=ctx + R)
+    kv = m.kv(ctx + R)
+    K, V = synth.kv_contents(one, 22, 0, ctx + R, dev)
+    kv.write(0, 0, K, V)
+    H, QD, F = one.hidden, one.n_q * 128, one.ffn
+    x = {"attn_norm": (H, H), "qkv_rope": (H, QD), "attention": (QD, QD), "o_residual": (QD, H),
+         "gate_up": (H, F), "down_residual": (F, H)}[args.op]
+    inp = synth.normal_bf16(5, 5, (R, x[0]), 1.0, dev)
+    out = synth.normal_bf16(6, 6, (R, x[1]), 1.0, dev)
+    for _ in range(args.warmup):
+        tfl.tfl_layer_op(m, args.op, 0, inp, out, kv, ctx)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(st)
+    for _ in range(args.steps):
+        tfl.tfl_layer_op(m, args.op, 0, inp, out, kv, ctx)
+    t1.record(st)
+    torch.cuda.synchronize()
+    us = t0.elapsed_time(t1) / args.steps * 1e3
+    wbytes = {"attn_norm": 2 * H, "qkv_rope": (QD + 2 * 1024) * H * 2, "attention": 2 * 1024 * 2 * (ctx + R),
+              "o_residual": H * QD * 2, "gate_up": 2 * F * H * 2, "down_residual": H * F * 2}[args.op]
+    print(json.dumps({"op": args.op, "rows": R, "context": ctx, "us_per_launch": round(us, 2),
+                      "bytes": wbytes, "gbs": round(wbytes / us / 1e3, 1)}), flush=True)
+
+
 def main():
     args = parse()
+    if args.op:
+        run_op(args)
+        return
     world, rank, local = dist_init(args)
     if args.impl == "reference":
         run_reference(args, world, rank)

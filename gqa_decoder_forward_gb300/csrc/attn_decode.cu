@@ -63,6 +63,9 @@ __device__ __forceinline__ bool find_group(const RowMap& m, int z, int& s, int& 
     return false;
 }
 
+// G = query heads per KV head (compile-time, so every per-pair loop has a fixed
+// length and the accumulators stay in registers).
+template <int G>
 __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_constant__ AttnDecodeArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
@@ -71,7 +74,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
     int s, r0, nr;
     if (!find_group(a.rows, blockIdx.z, s, r0, nr)) return;
     const int b = blockIdx.x, g = blockIdx.y;
-    const int G = a.n_q / a.n_kv;
     const int p_first = a.rows.pos0[s] + (r0 - a.rows.row_start[s]);
     const int p_last = p_first + nr - 1;
     const int k0 = b * kKB;
@@ -100,15 +102,18 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
     cp_async_wait_all();
     __syncthreads();
 
-    // scores: thread -> key t, half of the pairs
+    // scores: thread -> key t; the two thread halves split the G heads
     {
+        constexpr int GH = (G + 1) / 2;
         const int t = tid & (kKB - 1), half = tid >> 7;
-        const int ph = (P + 1) / 2;
-        const int pb = half * ph, pe = min(P, pb + ph);
-        float acc[(kMaxPairs + 1) / 2];
+        const int h0 = half * GH, hn = half ? G - GH : GH;
+        float acc[kRB][GH];
 #pragma unroll
-        for (int i = 0; i < (kMaxPairs + 1) / 2; ++i) acc[i] = 0.f;
+        for (int i = 0; i < kRB; ++i)
+#pragma unroll
+            for (int j = 0; j < GH; ++j) acc[i][j] = 0.f;
         if (t < nv) {
+#pragma unroll 2
             for (int d = 0; d < kHeadDim; d += 8) {
                 uint4 kw = *reinterpret_cast<const uint4*>(&sm.u.k[t][d]);
                 const bf16* kk = reinterpret_cast<const bf16*>(&kw);
@@ -116,21 +121,27 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
 #pragma unroll
                 for (int e = 0; e < 8; ++e) kf[e] = bf(kk[e]);
 #pragma unroll
-                for (int i = 0; i < (kMaxPairs + 1) / 2; ++i) {
-                    if (pb + i < pe) {
-                        const float* qq = &sm.q[pb + i][d];
+                for (int i = 0; i < kRB; ++i) {
+                    if (i < nr) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[i] = fmaf(qq[e], kf[e], acc[i]);
+                        for (int j = 0; j < GH; ++j) {
+                            if (j < hn) {
+                                const float* qq = &sm.q[i * G + h0 + j][d];
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) acc[i][j] = fmaf(qq[e], kf[e], acc[i][j]);
+                            }
+                        }
                     }
                 }
             }
         }
 #pragma unroll
-        for (int i = 0; i < (kMaxPairs + 1) / 2; ++i) {
-            const int p = pb + i;
-            if (p < pe) {
-                const int pos_row = p_first + p / G;
-                sm.s[p][t] = (t < nv && k0 + t <= pos_row) ? acc[i] : -INFINITY;
+        for (int i = 0; i < kRB; ++i) {
+            if (i < nr) {
+                const bool vis = t < nv && k0 + t <= p_first + i;
+#pragma unroll
+                for (int j = 0; j < GH; ++j)
+                    if (j < hn) sm.s[i * G + h0 + j][t] = vis ? acc[i][j] : -INFINITY;
             }
         }
     }
@@ -171,21 +182,30 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
     {
         const int d = tid & (kHeadDim - 1), half = tid >> 7;
         const int tb = half * (kKB / 2), te = min(nv, tb + kKB / 2);
-        float acc[kMaxPairs];
+        float acc[kRB][G];
 #pragma unroll
-        for (int p = 0; p < kMaxPairs; ++p) acc[p] = 0.f;
+        for (int i = 0; i < kRB; ++i)
+#pragma unroll
+            for (int j = 0; j < G; ++j) acc[i][j] = 0.f;
         for (int t = tb; t < te; ++t) {
             const float vv = bf(sm.v[t][d]);
 #pragma unroll
-            for (int p = 0; p < kMaxPairs; ++p) {
-                // a zero weight (a masked key) leaves the sum untouched, even its sign
-                const float w = sm.s[p][t];
-                if (p < P && w != 0.f) acc[p] = fmaf(w, vv, acc[p]);
+            for (int i = 0; i < kRB; ++i) {
+                if (i < nr) {
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        // a zero weight (a masked key) leaves the sum untouched, even its sign
+                        const float w = sm.s[i * G + j][t];
+                        if (w != 0.f) acc[i][j] = fmaf(w, vv, acc[i][j]);
+                    }
+                }
             }
         }
 #pragma unroll
-        for (int p = 0; p < kMaxPairs; ++p)
-            if (p < P) sm.u.red[half][p][d] = acc[p];
+        for (int i = 0; i < kRB; ++i)
+            if (i < nr)
+#pragma unroll
+                for (int j = 0; j < G; ++j) sm.u.red[half][i * G + j][d] = acc[i][j];
     }
     __syncthreads();
     pdl_trigger();
@@ -226,6 +246,7 @@ __global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const __grid_const
         __syncthreads();
         for (int b = d; b < n; b += kHeadDim) wts[b] = exp2f(a.pm[base + c + b] - M);
         __syncthreads();
+#pragma unroll 8
         for (int b = 0; b < n; ++b) {
             const float w = wts[b];
             L = fmaf(a.pl[base + c + b], w, L);
@@ -239,7 +260,10 @@ __global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const __grid_const
 }  // namespace
 
 cudaError_t init_attn_decode() {
-    return cudaFuncSetAttribute(attn_block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+    cudaError_t e = cudaFuncSetAttribute(attn_block_kernel<7>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(Smem));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(attn_block_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
 }
 
 int attn_decode_blocks(const AttnDecodeArgs& a, int* groups) {
@@ -255,7 +279,7 @@ int attn_decode_blocks(const AttnDecodeArgs& a, int* groups) {
 
 cudaError_t launch_attn_block(const AttnDecodeArgs& a, cudaStream_t st, bool pdl) {
     const int G = a.n_q / a.n_kv;
-    if (G > kMaxG || a.n_q % a.n_kv != 0) return cudaErrorInvalidValue;
+    if ((G != 7 && G != 8) || a.n_q % a.n_kv != 0) return cudaErrorInvalidValue;
     int groups = 0;
     const int nblk = attn_decode_blocks(a, &groups);
     if (nblk > a.max_blocks) return cudaErrorInvalidValue;
@@ -269,7 +293,7 @@ cudaError_t launch_attn_block(const AttnDecodeArgs& a, cudaStream_t st, bool pdl
     c1.stream = st;
     c1.attrs = attr;
     c1.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&c1, attn_block_kernel, a);
+    return G == 7 ? cudaLaunchKernelEx(&c1, attn_block_kernel<7>, a) : cudaLaunchKernelEx(&c1, attn_block_kernel<8>, a);
 }
 
 cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl) {

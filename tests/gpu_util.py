@@ -122,29 +122,49 @@ def oracle_chain(orc, shape, hw, layer, h_in, pos, K_prefix, V_prefix):
     ch["xn1"] = orc.rmsnorm(h_in, hw["attn_norm"][layer], shape.rms_eps)
     ch["qp"] = orc.linear(hw["wq"][layer], ch["xn1"]).reshape(R, shape.n_q, D)
     ch["kp"] = orc.linear(hw["wk"][layer], ch["xn1"]).reshape(R, shape.n_kv, D)
+    ch["qp_abs"] = orc.linear(abs_bits(hw["wq"][layer]), abs_bits(ch["xn1"])).reshape(R, shape.n_q, D)
+    ch["kp_abs"] = orc.linear(abs_bits(hw["wk"][layer]), abs_bits(ch["xn1"])).reshape(R, shape.n_kv, D)
     ch["q"] = orc.rope_apply(ch["qp"], pos, c, s)
     ch["k"] = orc.rope_apply(ch["kp"], pos, c, s)
     ch["v"] = orc.linear(hw["wv"][layer], ch["xn1"]).reshape(R, shape.n_kv, D)
+    ch["v_abs"] = orc.linear(abs_bits(hw["wv"][layer]), abs_bits(ch["xn1"])).reshape(R, shape.n_kv, D)
     P = K_prefix.shape[0]
     Kc = np.zeros((top, shape.n_kv, D), np.uint16)
     Vc = np.zeros_like(Kc)
     Kc[:P], Vc[:P] = K_prefix, V_prefix
     Kc[pos], Vc[pos] = ch["k"], ch["v"]
     ch["o"] = orc.attention(ch["q"], pos, Kc, Vc)
+    ch["o_abs"] = orc.attention(ch["q"], pos, Kc, abs_bits(Vc))     # sum p |v| / l
+    ch["n_keys"] = int(pos.max()) + 1
     ch["yo"] = orc.linear(hw["wo"][layer], ch["o"])
+    ch["yo_abs"] = orc.linear(abs_bits(hw["wo"][layer]), abs_bits(ch["o"]))
     ch["h1"] = orc.residual_add(h_in, ch["yo"])
     ch["y2"] = orc.rmsnorm(ch["h1"], ones_h, shape.rms_eps)
     ch["xn2"] = orc.rmsnorm(ch["h1"], hw["ffn_norm"][layer], shape.rms_eps)
     ch["g"] = orc.linear(hw["wg"][layer], ch["xn2"])
     ch["u"] = orc.linear(hw["wu"][layer], ch["xn2"])
+    ch["g_abs"] = orc.linear(abs_bits(hw["wg"][layer]), abs_bits(ch["xn2"]))
+    ch["u_abs"] = orc.linear(abs_bits(hw["wu"][layer]), abs_bits(ch["xn2"]))
     ch["sg"] = orc.swiglu(ch["g"], np.full_like(ch["g"], 0x3F80))   # bf16(silu(g))
     ch["a"] = orc.swiglu(ch["g"], ch["u"])
     ch["yd"] = orc.linear(hw["wd"][layer], ch["a"])
+    ch["yd_abs"] = orc.linear(abs_bits(hw["wd"][layer]), abs_bits(ch["a"]))
+    ch["K"] = (shape.hidden, shape.n_q * D, shape.ffn)
     ch["h2"] = orc.residual_add(ch["h1"], ch["yd"])
     return ch
 
 
 # ---- rounding-point bounds of the fused ops (all from oracle values) ---------------
+
+def abs_bits(b):
+    return np.asarray(b, np.uint16) & np.uint16(0x7FFF)
+
+
+def acc_allowance(abs_sum_bits, K):
+    """fp32 accumulation allowance of a K-term sum: sqrt(K) * 2^-24 * sum |terms|
+    (the usual probabilistic bound on rounding errors of a floating-point sum);
+    abs_sum_bits holds bf16(sum |terms|)."""
+    return np.sqrt(K) * 2.0 ** -24 * bf16_to_f64(abs_sum_bits)
 
 def _round_bits(v):
     f = np.asarray(v, np.float64).astype(np.float32)
@@ -157,31 +177,40 @@ def bound_norm(y, w, out):
     return ulp_of(out) + np.abs(bf16_to_f64(w)) * ulp_of(y)
 
 
-def bound_rope(pre, cos, sin, out):
-    """out_j = bf16(bf16(x_j c) + bf16(o_j s)) with x = pre (itself rounded), o the
-    rotate-half partner: ulp(out) + ulp of both products + |c| ulp(x_j) + |s| ulp(o_j)."""
+def bound_rope(pre, cos, sin, out, acc=0.0):
+    """out_j = bf16(bf16(x_j c) + bf16(o_j s)) with x = pre (a rounded sum with
+    accumulation allowance acc), o the rotate-half partner: ulp(out) + ulp of both
+    products + |c| (ulp(x_j) + acc_j) + |s| (ulp(o_j) + acc_o)."""
     x = bf16_to_f64(pre)
     half = x.shape[-1] // 2
     rot = np.concatenate([-x[..., half:], x[..., :half]], axis=-1)
     c = np.concatenate([bf16_to_f64(cos)] * 2, axis=-1)[:, None, :]
     s = np.concatenate([bf16_to_f64(sin)] * 2, axis=-1)[:, None, :]
-    ux = ulp_of(pre)
+    ux = ulp_of(pre) + acc
     urot = np.concatenate([ux[..., half:], ux[..., :half]], axis=-1)
     up = lambda v: ulp_of(_round_bits(v))  # noqa: E731
     return ulp_of(out) + up(x * c) + up(rot * s) + np.abs(c) * ux + np.abs(s) * urot
 
 
-def bound_residual(y, out):
-    """out = bf16(h + y), y itself rounded: ulp(out) + ulp(y)."""
-    return ulp_of(out) + ulp_of(y)
+def bound_residual(y, out, acc=0.0):
+    """out = bf16(h + y), y a rounded sum with accumulation allowance acc:
+    ulp(out) + ulp(y) + acc."""
+    return ulp_of(out) + ulp_of(y) + acc
 
 
-def bound_swiglu(g, u, sg, out):
-    """out = bf16(sg * u), sg = bf16(silu(g)), g and u rounded projections."""
+def bound_swiglu(g, u, sg, out, acc_g=0.0, acc_u=0.0):
+    """out = bf16(sg * u), sg = bf16(silu(g)), g and u rounded projections with
+    accumulation allowances acc_g, acc_u."""
     gv, uv, sv = bf16_to_f64(g), bf16_to_f64(u), bf16_to_f64(sg)
     sig = 1.0 / (1.0 + np.exp(-gv))
     dsilu = sig * (1.0 + gv * (1.0 - sig))
-    return ulp_of(out) + np.abs(uv) * ulp_of(sg) + np.abs(uv * dsilu) * ulp_of(g) + np.abs(sv) * ulp_of(u)
+    return (ulp_of(out) + np.abs(uv) * ulp_of(sg) + np.abs(uv * dsilu) * (ulp_of(g) + acc_g)
+            + np.abs(sv) * (ulp_of(u) + acc_u))
+
+
+def bound_sum(out, acc):
+    """A single rounded sum: ulp(out) + its accumulation allowance."""
+    return ulp_of(out) + acc
 
 
 def check_ops(tfl, model, kv, layer, ch, pos0, report=None, head=None):
@@ -205,27 +234,31 @@ def check_ops(tfl, model, kv, layer, ch, pos0, report=None, head=None):
     gate("attn_norm", out, ch["xn1"], bound_norm(ch["y1"], model_norm(model, "attn_norm", layer), ch["xn1"]))
     q = torch.empty_like(T(ch["q"]))
     tfl.tfl_layer_op(model, "qkv_rope", layer, T(ch["xn1"]), q, kv, pos0)
-    gate("qkv_rope.q", q, ch["q"], bound_rope(ch["qp"], ch["cos"], ch["sin"], ch["q"]))
+    H, QD, F = ch["K"]
+    gate("qkv_rope.q", q, ch["q"],
+         bound_rope(ch["qp"], ch["cos"], ch["sin"], ch["q"], acc_allowance(ch["qp_abs"], H)))
     k, v = kv.read(layer, pos0, R)
-    gate("qkv_rope.k", k, ch["k"], bound_rope(ch["kp"], ch["cos"], ch["sin"], ch["k"]))
-    gate("qkv_rope.v", v, ch["v"])
+    gate("qkv_rope.k", k, ch["k"],
+         bound_rope(ch["kp"], ch["cos"], ch["sin"], ch["k"], acc_allowance(ch["kp_abs"], H)))
+    gate("qkv_rope.v", v, ch["v"], bound_sum(ch["v"], acc_allowance(ch["v_abs"], H)))
     # the attention reads the oracle's keys and values for the call's own rows
     kv.write(layer, pos0, to_torch_bits(ch["k"]), to_torch_bits(ch["v"]))
     o = torch.empty_like(T(ch["o"]))
     tfl.tfl_layer_op(model, "attention", layer, T(ch["q"]), o, kv, pos0)
-    gate("attention", o, ch["o"])
+    gate("attention", o, ch["o"], bound_sum(ch["o"], acc_allowance(ch["o_abs"], ch["n_keys"])))
     h = T(ch["h_in"]).clone()
     tfl.tfl_layer_op(model, "o_residual", layer, T(ch["o"]), h)
-    gate("o_residual", h, ch["h1"], bound_residual(ch["yo"], ch["h1"]))
+    gate("o_residual", h, ch["h1"], bound_residual(ch["yo"], ch["h1"], acc_allowance(ch["yo_abs"], QD)))
     xn2 = torch.empty_like(h)
     tfl.tfl_layer_op(model, "ffn_norm", layer, T(ch["h1"]), xn2)
     gate("ffn_norm", xn2, ch["xn2"], bound_norm(ch["y2"], model_norm(model, "ffn_norm", layer), ch["xn2"]))
     a = torch.empty_like(T(ch["a"]))
     tfl.tfl_layer_op(model, "gate_up", layer, T(ch["xn2"]), a)
-    gate("gate_up", a, ch["a"], bound_swiglu(ch["g"], ch["u"], ch["sg"], ch["a"]))
+    gate("gate_up", a, ch["a"], bound_swiglu(ch["g"], ch["u"], ch["sg"], ch["a"], acc_allowance(ch["g_abs"], H),
+                                             acc_allowance(ch["u_abs"], H)))
     h = T(ch["h1"]).clone()
     tfl.tfl_layer_op(model, "down_residual", layer, T(ch["a"]), h)
-    gate("down_residual", h, ch["h2"], bound_residual(ch["yd"], ch["h2"]))
+    gate("down_residual", h, ch["h2"], bound_residual(ch["yd"], ch["h2"], acc_allowance(ch["yd_abs"], F)))
     if head is not None:
         orc, hw, shape = head
         ones_h = np.full(shape.hidden, 0x3F80, np.uint16)
@@ -236,7 +269,9 @@ def check_ops(tfl, model, kv, layer, ch, pos0, report=None, head=None):
         gate("final_norm", out, xnf, bound_norm(yf, hw["final_norm"], xnf))
         lg = torch.empty((R, shape.vocab), dtype=torch.bfloat16, device="cuda")
         tfl.tfl_layer_op(model, "lm_head", 0, T(xnf), lg)
-        gate("lm_head", lg, orc.linear(hw["lm_head"], xnf))
+        lm = orc.linear(hw["lm_head"], xnf)
+        lm_abs = orc.linear(abs_bits(hw["lm_head"]), abs_bits(xnf))
+        gate("lm_head", lg, lm, bound_sum(lm, acc_allowance(lm_abs, shape.hidden)))
     torch.cuda.synchronize()
     if report is not None:
         report.update(res)
