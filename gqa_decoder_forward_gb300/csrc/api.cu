@@ -417,6 +417,24 @@ int prefill_common(tfl_model* m, tfl_kv* kv, const int32_t* ids, const void* h_i
 
 }  // namespace
 
+// ---- helpers for entry points defined in other files ---------------------------------
+
+namespace tfl {
+
+int kv_handle_view(const tfl_kv* kv, KvView* out, int* max_pos, int* n_q, int* n_kv, int* layers) {
+    if (!kv || !kv->model) return TFL_E_ARG;
+    *out = view(kv);
+    *max_pos = kv->max_pos;
+    *n_q = kv->model->cfg.n_q;
+    *n_kv = kv->model->cfg.n_kv;
+    *layers = kv->model->cfg.layers;
+    return TFL_OK;
+}
+
+void set_last_error(const char* msg) { g_err = msg; }
+
+}  // namespace tfl
+
 // ---- C ABI ------------------------------------------------------------------------
 
 extern "C" {

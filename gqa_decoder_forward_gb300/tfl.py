@@ -75,6 +75,7 @@ SIGNATURES = {
     "tfl_head": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _vp, _vp]),
     "tfl_layer_op": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int, _vp, _vp,
                                     _vp]),
+    "tfl_attention_decode_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp]),
     "tfl_profile": (ctypes.c_int, [_vp, ctypes.c_int]),
     "tfl_profile_read": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_long)]),
@@ -288,6 +289,12 @@ def tfl_layer_op(model: Model, op: str, layer: int, inp: torch.Tensor, out: torc
                  pos0: int = 0, stream=None):
     return _check(lib().tfl_layer_op(model.handle, OPS[op], layer, kv.handle if kv is not None else None, pos0,
                                      inp.shape[0], _ptr(inp), _ptr(out), _stream(stream)))
+
+
+def tfl_attention_decode_noalloc(kv: "KV", layer: int, pos0: int, q: torch.Tensor, out: torch.Tensor, stream=None):
+    """Decode attention with the library's fixed scratch (no allocation, no workspace)."""
+    return _check(lib().tfl_attention_decode_noalloc(kv.handle, layer, pos0, q.shape[0], _ptr(q), _ptr(out),
+                                                     _stream(stream)))
 
 
 def tfl_profile(model: Model, enable: bool):

@@ -267,6 +267,29 @@ int tfl_head(tfl_model* model, const void* h, int rows, void* logits, void* stre
 int tfl_layer_op(tfl_model* model, int op, int layer, tfl_kv* kv, int pos0, int rows, const void* in, void* out,
                  void* stream);
 
+/*
+ * Decode attention that allocates nothing and needs no workspace.  The pages
+ * have no counterpart: this is a convenience for callers that cannot allocate
+ * device memory where they run attention (a serving runtime whose memory
+ * manager owns all of the GPU's memory, or code that must not call cudaMalloc
+ * because it can synchronise the device or break a stream capture).
+ * Same computation and kernels as TFL_OP_ATTENTION of tfl_layer_op: rows
+ * (1..64) of rotated queries q (device bf16 [rows][n_q*D]) at positions pos0 ..
+ * pos0+rows-1 attend keys 0..pos0+i of kv (layer); out is device bf16
+ * [rows][n_q*D].  The softmax partials live in a fixed 16 MiB array inside the
+ * library (held on every GPU that loads it until the process exits):
+ * rows * n_q * ceil((pos0+rows)/128) must not exceed 32,263 (for the 33B shape:
+ * one row up to 73,728 positions, 16 rows up to 4,608), else TFL_E_WORKSPACE
+ * with a message.  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the array: calls that overlap on
+ * the GPU race, so serialise them (one stream, or events).  It needs no
+ * clearing between calls.  Calls no cudaMalloc, cudaFree or allocating library
+ * routine.
+ */
+int tfl_attention_decode_noalloc(tfl_kv* kv, int layer, int pos0, int rows, const void* q, void* out,
+                                 void* stream);
+
 /* ---- per-kernel timing ------------------------------------------------------------- */
 
 /*
