@@ -6,8 +6,11 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
+
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "../../include/tfl.h"
@@ -91,6 +94,7 @@ struct Layout {
     int max_blocks;
 };
 
+
 Layout layout(const tfl_config* c) {
     Layout L;
     const size_t rows = (size_t)std::max(c->max_rows, c->max_decode_rows);
@@ -136,6 +140,45 @@ uint16_t host_bf16(double x) {
     return (uint16_t)(b >> 16);
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// A 3-D bf16 tensor map over a row-major [rows][K] matrix viewed as (64
+// columns, rows, K/64 k-blocks) -- strides K*2 and 128 bytes -- with 128-byte
+// swizzle and boxes of (64, box_rows, 8).
+bool encode_map(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn || ((uintptr_t)ptr & 15u) || K % 64 != 0 || box_rows < 1 || box_rows > 256) return false;
+    cuuint64_t dims[3] = {64, rows, K / 64};
+    cuuint64_t strides[2] = {K * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, 8};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Index of the activation-row box for a call of `rows` rows: 1..8 -> 0..7,
+// 16 -> 8, 32 -> 9, 64 -> 10.
+int xbox_index(int rows) {
+    const int xr = matvec_tma_x_rows(rows);
+    return xr <= 8 ? xr - 1 : xr == 16 ? 8 : xr == 32 ? 9 : 10;
+}
+constexpr int kXBoxes = 11;
+
 }  // namespace
 
 // ---- model / kv objects --------------------------------------------------------
@@ -161,6 +204,14 @@ struct tfl_model {
     float *pm, *pl, *po;
     int* status;
     bool pdl;
+    // TMA descriptors of every projection and of the activation buffers
+    struct LayerMaps {
+        CUtensorMap q, k, v, o, g, u, d;
+    };
+    std::vector<LayerMaps> wmaps;
+    CUtensorMap lm_map;
+    CUtensorMap xmap_xn[kXBoxes], xmap_ao[kXBoxes], xmap_act[kXBoxes];  // by xbox_index(rows)
+    int grid = 0;
     bool prof = false;
     std::vector<Mark> marks;         // recorded while profiling
     std::vector<cudaEvent_t> spare;  // event pool
@@ -224,6 +275,24 @@ KvView view(const tfl_kv* kv) {
     return v;
 }
 
+// Launches the TMA matvec with weight maps w0..w2 and activation map xm (whose
+// box rows must be matvec_tma_x_rows(e.n_rows)).
+cudaError_t mv_launch(tfl_model* m, const MatvecArgs& e, const CUtensorMap* w0, const CUtensorMap* w1,
+                      const CUtensorMap* w2, const CUtensorMap* xm, cudaStream_t st, bool pdl) {
+    MatvecTmaArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.e = e;
+    a.wmap[0] = *w0;
+    if (w1) a.wmap[1] = *w1;
+    if (w2) a.wmap[2] = *w2;
+    a.xmap = *xm;
+    a.x_rows_box = matvec_tma_x_rows(e.n_rows);
+    a.tiles = matvec_tma_tiles(e);
+    a.kstages = (e.K + 511) / 512;
+    a.status = m->status;
+    return launch_matvec_tma(a, m->grid, st, pdl);
+}
+
 // The layer stack over n rows described by rm (decode kernels).  Input: ids
 // (embedding gather) or h_in; output: the residual stream in m->h.
 int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h_in, cudaStream_t st) {
@@ -256,7 +325,9 @@ int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h
         a.sin_t = m->sin_t;
         a.layer = l;
         a.rows = rm;
-        LAUNCH(m, K_QKV, st, launch_matvec(a, st, pdl));
+        const int xi = xbox_index(n);
+        const tfl_model::LayerMaps& wm = m->wmaps[l];
+        LAUNCH(m, K_QKV, st, mv_launch(m, a, &wm.q, &wm.k, &wm.v, &m->xmap_xn[xi], st, pdl));
 
         AttnDecodeArgs at = {};
         at.q = m->q;
@@ -280,7 +351,7 @@ int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h
         o.w0 = m->wo[l];
         o.n_out = H;
         o.h = m->h;
-        LAUNCH(m, K_O, st, launch_matvec(o, st, pdl));
+        LAUNCH(m, K_O, st, mv_launch(m, o, &wm.o, nullptr, nullptr, &m->xmap_ao[xi], st, pdl));
 
         LAUNCH(m, K_NORM, st, launch_rmsnorm(m->h, m->ffn_norm[l], c.rms_eps, n, H, m->xn, st, pdl));
 
@@ -294,7 +365,7 @@ int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h
         gu.n_out = c.ffn;
         gu.y = m->act;
         gu.ldy = c.ffn;
-        LAUNCH(m, K_GATEUP, st, launch_matvec(gu, st, pdl));
+        LAUNCH(m, K_GATEUP, st, mv_launch(m, gu, &wm.g, &wm.u, nullptr, &m->xmap_xn[xi], st, pdl));
 
         MatvecArgs d = {};
         d.mode = MV_RESIDUAL;
@@ -304,7 +375,7 @@ int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h
         d.w0 = m->wd[l];
         d.n_out = H;
         d.h = m->h;
-        LAUNCH(m, K_DOWN, st, launch_matvec(d, st, pdl));
+        LAUNCH(m, K_DOWN, st, mv_launch(m, d, &wm.d, nullptr, nullptr, &m->xmap_act[xi], st, pdl));
     }
     return TFL_OK;
 }
@@ -326,7 +397,8 @@ int run_head(tfl_model* m, int r0, int n, void* logits, long ld_rows_out, cudaSt
         a.n_out = c.vocab;
         a.y = (bf16*)logits + (size_t)b * ld_rows_out;
         a.ldy = ld_rows_out;
-        LAUNCH(m, K_LMHEAD, st, launch_matvec(a, st, m->pdl && st != nullptr));
+        LAUNCH(m, K_LMHEAD, st, mv_launch(m, a, &m->lm_map, nullptr, nullptr, &m->xmap_xn[xbox_index(k)], st,
+                                          m->pdl && st != nullptr));
     }
     return TFL_OK;
 }
@@ -537,6 +609,35 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
     m->status = (int*)(m->ws + L.status);
     m->pdl = true;
 
+    // projections: TMA descriptors of every weight matrix and activation buffer
+    {
+        const int H = cfg->hidden, QD = cfg->n_q * kHeadDim, KD = cfg->n_kv * kHeadDim, F = cfg->ffn;
+        const size_t rows = (size_t)std::max(cfg->max_rows, cfg->max_decode_rows);
+        bool okm = true;
+        m->wmaps.resize(cfg->layers);
+        for (int l = 0; l < cfg->layers && okm; ++l) {
+            tfl_model::LayerMaps& x = m->wmaps[l];
+            okm = encode_map(&x.q, m->wq[l], H, QD, 8) && encode_map(&x.k, m->wk[l], H, KD, 8) &&
+                  encode_map(&x.v, m->wv[l], H, KD, 8) && encode_map(&x.o, m->wo[l], QD, H, 16) &&
+                  encode_map(&x.g, m->wg[l], H, F, 8) && encode_map(&x.u, m->wu[l], H, F, 8) &&
+                  encode_map(&x.d, m->wd[l], F, H, 16);
+        }
+        okm = okm && encode_map(&m->lm_map, m->lm_head, H, cfg->vocab, 16);
+        const int xrows[kXBoxes] = {1, 2, 3, 4, 5, 6, 7, 8, 16, 32, 64};
+        for (int i = 0; i < kXBoxes && okm; ++i)
+            okm = encode_map(&m->xmap_xn[i], m->xn, H, rows, xrows[i]) &&
+                  encode_map(&m->xmap_ao[i], m->ao, QD, rows, xrows[i]) &&
+                  encode_map(&m->xmap_act[i], m->act, F, rows, xrows[i]);
+        cudaError_t ce0 = cudaSuccess;
+        if (okm) ce0 = init_matvec_tma();
+        if (!okm || ce0 != cudaSuccess) {
+            delete m;
+            return fail(TFL_E_CUDA, "building TMA descriptors failed%s%s", ce0 ? ": " : "",
+                        ce0 ? cudaGetErrorString(ce0) : "");
+        }
+        m->grid = prop.multiProcessorCount;
+    }
+
     std::vector<uint16_t> c((size_t)cfg->max_context * 64), s((size_t)cfg->max_context * 64);
     tfl_rope_table(cfg->rope_theta, cfg->max_context, c.data(), s.data());
     cudaError_t ce = cudaMemcpy(m->cos_t, c.data(), c.size() * 2, cudaMemcpyHostToDevice);
@@ -687,6 +788,11 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
     MatvecArgs a = {};
     a.n_rows = rows;
     a.x = (const bf16*)in;
+    // the caller's activation rows as a TMA source (rows beyond `rows` read as zeros)
+    CUtensorMap xm;
+    auto xmap = [&](int K) {
+        return encode_map(&xm, in, (uint64_t)K, (uint64_t)rows, (uint32_t)matvec_tma_x_rows(rows));
+    };
     switch (op) {
         case TFL_OP_ATTN_NORM:
         case TFL_OP_FFN_NORM:
@@ -710,7 +816,9 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.sin_t = m->sin_t;
             a.layer = layer;
             a.rows = rm;
-            LAUNCH(m, K_QKV, st, launch_matvec(a, st, false));
+            if (!xmap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
+            LAUNCH(m, K_QKV, st,
+                   mv_launch(m, a, &m->wmaps[layer].q, &m->wmaps[layer].k, &m->wmaps[layer].v, &xm, st, false));
             break;
         case TFL_OP_ATTENTION: {
             AttnDecodeArgs at = {};
@@ -735,7 +843,10 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.w0 = op == TFL_OP_O_RESIDUAL ? m->wo[layer] : m->wd[layer];
             a.n_out = H;
             a.h = (bf16*)out;
-            LAUNCH(m, op == TFL_OP_O_RESIDUAL ? K_O : K_DOWN, st, launch_matvec(a, st, false));
+            if (!xmap(a.K)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
+            LAUNCH(m, op == TFL_OP_O_RESIDUAL ? K_O : K_DOWN, st,
+                   mv_launch(m, a, op == TFL_OP_O_RESIDUAL ? &m->wmaps[layer].o : &m->wmaps[layer].d, nullptr,
+                             nullptr, &xm, st, false));
             break;
         case TFL_OP_GATE_UP:
             a.mode = MV_SWIGLU;
@@ -745,7 +856,9 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.n_out = c.ffn;
             a.y = (bf16*)out;
             a.ldy = c.ffn;
-            LAUNCH(m, K_GATEUP, st, launch_matvec(a, st, false));
+            if (!xmap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
+            LAUNCH(m, K_GATEUP, st,
+                   mv_launch(m, a, &m->wmaps[layer].g, &m->wmaps[layer].u, nullptr, &xm, st, false));
             break;
         case TFL_OP_LM_HEAD:
             a.mode = MV_STORE;
@@ -754,7 +867,8 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.n_out = c.vocab;
             a.y = (bf16*)out;
             a.ldy = c.vocab;
-            LAUNCH(m, K_LMHEAD, st, launch_matvec(a, st, false));
+            if (!xmap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
+            LAUNCH(m, K_LMHEAD, st, mv_launch(m, a, &m->lm_map, nullptr, nullptr, &xm, st, false));
             break;
     }
     return ok();

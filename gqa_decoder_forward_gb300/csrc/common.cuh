@@ -1,6 +1,7 @@
 // Internal declarations shared by the sm_103a kernels and the host orchestrator.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -69,8 +70,8 @@ struct MatvecArgs {
     int K;                 // reduction length (multiple of 256)
     int n_rows;            // activation rows, 1..64
     const bf16* x;         // [n_rows][K]
-    // weights: STORE/RESIDUAL use w0 ([N][K]); SWIGLU w0 = gate, w1 = up ([F][K]);
-    // QKV_ROPE w0 = Wq, w1 = Wk, w2 = Wv.
+    // weights (the TMA kernel reads them through its tensor maps): STORE/RESIDUAL
+    // w0 ([N][K]); SWIGLU w0 = gate, w1 = up ([F][K]); QKV_ROPE w0 = Wq, w1 = Wk, w2 = Wv.
     const bf16* w0;
     const bf16* w1;
     const bf16* w2;
@@ -84,7 +85,25 @@ struct MatvecArgs {
     int layer;             // QKV: cache layer
     RowMap rows;           // QKV: positions and caches of the rows
 };
-cudaError_t launch_matvec(const MatvecArgs& a, cudaStream_t st, bool pdl);
+
+// The TMA-fed variant: weights through 3-D tensor maps over [N][K] viewed as
+// (64 columns, rows, K/64 k-blocks) with 128-byte swizzle and boxes of
+// (64, 16 or 8 rows, 8 k-blocks); activation rows likewise with boxes of
+// (64, x_rows_box, 8).
+struct MatvecTmaArgs {
+    MatvecArgs e;           // mode, K, n_rows, epilogue outputs, positions
+    CUtensorMap wmap[3];    // STORE/RESIDUAL [0] (16-row boxes); SWIGLU gate, up; QKV q, k, v (8-row boxes)
+    CUtensorMap xmap;       // activation rows, box rows = x_rows_box
+    int x_rows_box;         // n_rows for n_rows <= 8, else 8 * NT
+    int tiles;              // tiles of 16 weight rows
+    int kstages;            // ceil(K / 512)
+    int* status;
+};
+int matvec_tma_nt(int n_rows);
+int matvec_tma_x_rows(int n_rows);
+int matvec_tma_tiles(const MatvecArgs& e);
+cudaError_t init_matvec_tma();
+cudaError_t launch_matvec_tma(const MatvecTmaArgs& a, int grid, cudaStream_t st, bool pdl);
 
 cudaError_t launch_embed_rmsnorm(const int32_t* ids, const bf16* embed, int vocab, const bf16* w, float eps,
                                  int n_rows, int H, bf16* h, bf16* xn, int* status, cudaStream_t st, bool pdl);
