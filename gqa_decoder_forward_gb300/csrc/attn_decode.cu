@@ -5,47 +5,77 @@
 //
 // Pass 1 (attn_block_kernel): one CTA per (key block b of 128 positions, KV
 // head g, group of <= 4 rows of one stream).  The block's keys and values for
-// head g are staged in shared memory with cp.async, the G = n_q/n_kv query
-// heads of each row read them, and the CTA writes per (row, head) the block's
-// max score m_b, sum l_b = sum exp(s - m_b) and o_b = sum exp(s - m_b) v.
+// head g are staged in shared memory with cp.async.  The G = n_q/n_kv query
+// heads of the group's rows form the M dimension of tensor-core products
+// (mma.sync m16n8k16, bf16 in, fp32 accumulate): S = Q K^T over the 128 keys,
+// then O = P V.  Per (row, head) the CTA writes the block's max score m_b, sum
+// l_b = sum exp(s - m_b) and o_b = sum exp(s - m_b) v.
 // Pass 2 (attn_merge_kernel): per (row, head), M = max_b m_b, then
 // L = sum_b l_b e^(m_b - M) and O = sum_b o_b e^(m_b - M) in block order,
 // out = bf16(O / L).
 //
-// Scores are fp32 dot products in d order of q (pre-scaled by log2(e)/sqrt(D))
-// with the bf16 keys; softmax weights stay fp32 (never rounded to bf16).
-// Every row's arithmetic depends only on its own position: the block split is
-// fixed by absolute position and masked keys contribute exact zeros, so a row
-// gives the same bits alone or beside other rows (one-row steps == windows).
+// Precision: scores are fp32 dot products of the bf16 q and k, scaled in fp32;
+// softmax weights are fp32 and enter P V as a pair of bf16 numbers
+// (hi = bf16(p), lo = bf16(p - hi)), i.e. with about 16 significant bits --
+// the weights are not rounded to bf16.
+//
+// Determinism: every row's arithmetic depends only on its own position: the
+// block split is fixed by absolute position, masked keys have weight exactly
+// 0, keys past the last one any row of the group sees are zero-filled in
+// shared memory, and each output element of an mma depends only on its own
+// row of P.  A row gives the same bits alone or beside other rows (one-row
+// steps == windows, solo == batched).
 #include "common.cuh"
 
 namespace tfl {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRB = 4;          // rows per CTA
-constexpr int kKB = kPage;      // keys per block
-constexpr int kKPad = kHeadDim + 8;  // padded key row in shared memory (bf16)
-constexpr int kMaxG = 8;        // query heads per KV head
-constexpr int kMaxPairs = kRB * kMaxG;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRB = 4;               // rows per CTA
+constexpr int kKB = kPage;           // keys per block
+constexpr int kPad = kHeadDim + 8;   // padded row (bf16): 272 bytes, conflict-free ldmatrix
+constexpr int kMaxPairs = 32;        // kRB rows x up to 8 heads, two m16 tiles
 
 struct Smem {
-    float q[kMaxPairs][kHeadDim];          // 16 KB
-    float s[kMaxPairs][kKB];               // 16 KB scores, then weights
-    union {
-        bf16 k[kKB][kKPad];                // 34 KB
-        float red[2][kMaxPairs][kHeadDim]; // 32 KB (after the scores)
-    } u;
-    bf16 v[kKB][kHeadDim];                 // 32 KB
-    float m[kMaxPairs];
-    float l[kMaxPairs];
+    bf16 q[kMaxPairs][kPad];         // 8.5 KB
+    bf16 k[kKB][kPad];               // 34 KB
+    bf16 v[kKB][kPad];               // 34 KB
+    bf16 p[2][kMaxPairs][kPad];      // 17 KB: softmax weights, hi and lo parts
+    float wmax[kWarps][kMaxPairs];   // per-warp row maxima
+    float wsum[kWarps][kMaxPairs];   // per-warp row sums
 };
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-    unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem));
+__device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, bool valid) {
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    const int src = valid ? 16 : 0;  // 0 source bytes: the 16 destination bytes are zero-filled
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gmem), "r"(src));
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(bf16 lo, bf16 hi) {
+    return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+}
 
 // Locates row group z: stream s, first row (global index) r0, row count nr.
 __device__ __forceinline__ bool find_group(const RowMap& m, int z, int& s, int& r0, int& nr) {
@@ -63,8 +93,7 @@ __device__ __forceinline__ bool find_group(const RowMap& m, int z, int& s, int& 
     return false;
 }
 
-// G = query heads per KV head (compile-time, so every per-pair loop has a fixed
-// length and the accumulators stay in registers).
+// G = query heads per KV head.  Pair p = i*G + j is (row i of the group, head g*G + j).
 template <int G>
 __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_constant__ AttnDecodeArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -79,149 +108,183 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
     const int k0 = b * kKB;
     if (k0 > p_last) return;
     const int nv = min(kKB, p_last + 1 - k0);  // keys of this block any row sees
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gq = lane >> 2, tig = lane & 3;
+    const int P = nr * G;
+    const int MT = (P + 15) / 16;  // m16 tiles of pairs
 
-    // stage keys and values of head g (rows of 256 B inside one page)
+    // stage keys and values of head g (rows of 256 B inside one page); keys past
+    // nv are zero-filled so that their weight-0 products stay exact zeros
     const KvView& kv = a.rows.kv[s];
     const bf16* kbase = kv_row(kv, a.layer, 0, k0, a.n_kv) + (size_t)g * kHeadDim;
     const bf16* vbase = kv_row(kv, a.layer, 1, k0, a.n_kv) + (size_t)g * kHeadDim;
     const size_t pstride = (size_t)a.n_kv * kHeadDim;
-    for (int i = tid; i < nv * 16; i += kThreads) {
-        int t = i >> 4, c = i & 15;
-        cp_async16(&sm.u.k[t][c * 8], kbase + t * pstride + c * 8);
-        cp_async16(&sm.v[t][c * 8], vbase + t * pstride + c * 8);
+    for (int i = tid; i < kKB * 16; i += kThreads) {
+        const int t = i >> 4, c = i & 15;
+        const bool valid = t < nv;
+        const size_t off = valid ? t * pstride + c * 8 : 0;
+        cp_async16_zfill(&sm.k[t][c * 8], kbase + off, valid);
+        cp_async16_zfill(&sm.v[t][c * 8], vbase + off, valid);
     }
-    // queries, pre-scaled: pair p = i*G + hh (row i of the group, head g*G + hh)
-    const int P = nr * G;
-    const float qscale = 1.4426950408889634f * rsqrtf((float)kHeadDim);
-    for (int i = tid; i < P * kHeadDim; i += kThreads) {
-        int p = i / kHeadDim, d = i % kHeadDim;
-        int row = r0 + p / G, head = g * G + p % G;
-        sm.q[p][d] = bf(a.q[(size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + d]) * qscale;
+    // queries (bf16, unscaled); pairs past P are zero
+    for (int i = tid; i < MT * 16 * 16; i += kThreads) {
+        const int p = i >> 4, c = i & 15;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (p < P) {
+            const int row = r0 + p / G, head = g * G + p % G;
+            val = *reinterpret_cast<const uint4*>(a.q + (size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim +
+                                                   c * 8);
+        }
+        *reinterpret_cast<uint4*>(&sm.q[p][c * 8]) = val;
     }
     cp_async_wait_all();
     __syncthreads();
 
-    // scores: thread -> key t; the two thread halves split the G heads
+    // ---- S = Q K^T: warp w owns keys 16w .. 16w+15 (two n8 tiles) ----
+    const float kScale = 0.12751743074640502f;  // log2(e) / sqrt(128)
+    float sc[2][2][4];  // [m tile][n tile][fragment]
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
     {
-        constexpr int GH = (G + 1) / 2;
-        const int t = tid & (kKB - 1), half = tid >> 7;
-        const int h0 = half * GH, hn = half ? G - GH : GH;
-        float acc[kRB][GH];
+        const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8, mcol = (lane >> 4) * 8;     // A: matrices (r, k) quads
+        const int krow = (lane & 7) + (lane >> 4) * 8, kcol = ((lane >> 3) & 1) * 8;     // B: keys x dims
 #pragma unroll
-        for (int i = 0; i < kRB; ++i)
+        for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+            uint32_t bk[4];
+            ldsm_x4(bk, &sm.k[warp * 16 + krow][ks * 16 + kcol]);
 #pragma unroll
-            for (int j = 0; j < GH; ++j) acc[i][j] = 0.f;
-        if (t < nv) {
+            for (int mt = 0; mt < 2; ++mt) {
+                if (mt < MT) {
+                    uint32_t aq[4];
+                    ldsm_x4(aq, &sm.q[mt * 16 + mrow][ks * 16 + mcol]);
+                    mma16816(sc[mt][0], aq, bk[0], bk[1]);
+                    mma16816(sc[mt][1], aq, bk[2], bk[3]);
+                }
+            }
+        }
+    }
+    // scale, mask, per-warp row maxima
+    float mx[2][2];  // [m tile][row half]
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int p = mt * 16 + gq + h * 8;
+            const int pos_row = p_first + (p < P ? p / G : 0);
+            float m = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int t = warp * 16 + nt * 8 + 2 * tig + e;
+                    const bool vis = p < P && t < nv && k0 + t <= pos_row;
+                    float& v = sc[mt][nt][h * 2 + e];
+                    v = vis ? v * kScale : -INFINITY;
+                    m = fmaxf(m, v);
+                }
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            mx[mt][h] = m;
+        }
+    }
+    if (tig == 0) {
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) sm.wmax[warp][mt * 16 + gq + h * 8] = mx[mt][h];
+    }
+    __syncthreads();
+    // block row maxima, weights, per-warp row sums, weights to shared memory
+    float bmax[2][2];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int p = mt * 16 + gq + h * 8;
+            float m = sm.wmax[0][p];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) m = fmaxf(m, sm.wmax[w][p]);
+            bmax[mt][h] = m;
+            float l = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                float e0 = 0.f, e1 = 0.f;
+                if (m != -INFINITY) {
+                    e0 = exp2f(sc[mt][nt][h * 2 + 0] - m);
+                    e1 = exp2f(sc[mt][nt][h * 2 + 1] - m);
+                }
+                l += e0;
+                l += e1;
+                const bf16 h0 = rn(e0), h1 = rn(e1);
+                const bf16 l0 = rn(e0 - bf(h0)), l1 = rn(e1 - bf(h1));
+                const int t = warp * 16 + nt * 8 + 2 * tig;
+                *reinterpret_cast<uint32_t*>(&sm.p[0][p][t]) = pack_bf16(h0, h1);
+                *reinterpret_cast<uint32_t*>(&sm.p[1][p][t]) = pack_bf16(l0, l1);
+            }
+            l += __shfl_xor_sync(0xffffffffu, l, 1);
+            l += __shfl_xor_sync(0xffffffffu, l, 2);
+            if (tig == 0) sm.wsum[warp][p] = l;
+        }
+    }
+    __syncthreads();
+
+    // ---- O = P V: warp w owns dims 16w .. 16w+15 (two n8 tiles) ----
+    float oc[2][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) oc[mt][nt][0] = oc[mt][nt][1] = oc[mt][nt][2] = oc[mt][nt][3] = 0.f;
+    {
+        const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8, mcol = (lane >> 4) * 8;  // A: pairs x keys
+        const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8, vcol = (lane >> 4) * 8;  // B (trans): keys x dims
 #pragma unroll 2
-            for (int d = 0; d < kHeadDim; d += 8) {
-                uint4 kw = *reinterpret_cast<const uint4*>(&sm.u.k[t][d]);
-                const bf16* kk = reinterpret_cast<const bf16*>(&kw);
-                float kf[8];
+        for (int ks = 0; ks < kKB / 16; ++ks) {
+            uint32_t bv[4];
+            ldsm_x4_t(bv, &sm.v[ks * 16 + vrow][warp * 16 + vcol]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) kf[e] = bf(kk[e]);
+            for (int mt = 0; mt < 2; ++mt) {
+                if (mt < MT) {
 #pragma unroll
-                for (int i = 0; i < kRB; ++i) {
-                    if (i < nr) {
-#pragma unroll
-                        for (int j = 0; j < GH; ++j) {
-                            if (j < hn) {
-                                const float* qq = &sm.q[i * G + h0 + j][d];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) acc[i][j] = fmaf(qq[e], kf[e], acc[i][j]);
-                            }
-                        }
+                    for (int part = 0; part < 2; ++part) {
+                        uint32_t ap[4];
+                        ldsm_x4(ap, &sm.p[part][mt * 16 + mrow][ks * 16 + mcol]);
+                        mma16816(oc[mt][0], ap, bv[0], bv[1]);
+                        mma16816(oc[mt][1], ap, bv[2], bv[3]);
                     }
                 }
             }
         }
-#pragma unroll
-        for (int i = 0; i < kRB; ++i) {
-            if (i < nr) {
-                const bool vis = t < nv && k0 + t <= p_first + i;
-#pragma unroll
-                for (int j = 0; j < GH; ++j)
-                    if (j < hn) sm.s[i * G + h0 + j][t] = vis ? acc[i][j] : -INFINITY;
-            }
-        }
     }
-    __syncthreads();
-
-    // softmax statistics of the block: warp per pair, lane per 4 keys
-    {
-        const int warp = tid >> 5, lane = tid & 31;
-        for (int p = warp; p < P; p += kThreads / 32) {
-            float x0 = sm.s[p][lane * 4 + 0], x1 = sm.s[p][lane * 4 + 1];
-            float x2 = sm.s[p][lane * 4 + 2], x3 = sm.s[p][lane * 4 + 3];
-            float m = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            float e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
-            if (m != -INFINITY) {
-                e0 = exp2f(x0 - m);
-                e1 = exp2f(x1 - m);
-                e2 = exp2f(x2 - m);
-                e3 = exp2f(x3 - m);
-            }
-            float l = ((e0 + e1) + e2) + e3;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-            sm.s[p][lane * 4 + 0] = e0;
-            sm.s[p][lane * 4 + 1] = e1;
-            sm.s[p][lane * 4 + 2] = e2;
-            sm.s[p][lane * 4 + 3] = e3;
-            if (lane == 0) {
-                sm.m[p] = m;
-                sm.l[p] = l;
-            }
-        }
-    }
-    __syncthreads();
-
-    // P.V: thread -> dim d, half of the keys; halves added in order
-    {
-        const int d = tid & (kHeadDim - 1), half = tid >> 7;
-        const int tb = half * (kKB / 2), te = min(nv, tb + kKB / 2);
-        float acc[kRB][G];
-#pragma unroll
-        for (int i = 0; i < kRB; ++i)
-#pragma unroll
-            for (int j = 0; j < G; ++j) acc[i][j] = 0.f;
-        for (int t = tb; t < te; ++t) {
-            const float vv = bf(sm.v[t][d]);
-#pragma unroll
-            for (int i = 0; i < kRB; ++i) {
-                if (i < nr) {
-#pragma unroll
-                    for (int j = 0; j < G; ++j) {
-                        // a zero weight (a masked key) leaves the sum untouched, even its sign
-                        const float w = sm.s[i * G + j][t];
-                        if (w != 0.f) acc[i][j] = fmaf(w, vv, acc[i][j]);
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < kRB; ++i)
-            if (i < nr)
-#pragma unroll
-                for (int j = 0; j < G; ++j) sm.u.red[half][i * G + j][d] = acc[i][j];
-    }
-    __syncthreads();
     pdl_trigger();
 
-    for (int i = tid; i < P * kHeadDim; i += kThreads) {
-        const int p = i / kHeadDim, d = i % kHeadDim;
-        const int row = r0 + p / G, head = g * G + p % G;
-        const size_t idx = ((size_t)row * a.n_q + head) * a.max_blocks + b;
-        a.po[idx * kHeadDim + d] = sm.u.red[0][p][d] + sm.u.red[1][p][d];
-        if (d == 0) {
-            a.pm[idx] = sm.m[p];
-            a.pl[idx] = sm.l[p];
+    // ---- partials: o (unnormalised), m, l per (row, head) ----
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int p = mt * 16 + gq + h * 8;
+            if (mt < MT && p < P) {
+                const int row = r0 + p / G, head = g * G + p % G;
+                const size_t idx = ((size_t)row * a.n_q + head) * a.max_blocks + b;
+                float* po = a.po + idx * kHeadDim + warp * 16 + 2 * tig;
+                *reinterpret_cast<float2*>(po) = make_float2(oc[mt][0][h * 2 + 0], oc[mt][0][h * 2 + 1]);
+                *reinterpret_cast<float2*>(po + 8) = make_float2(oc[mt][1][h * 2 + 0], oc[mt][1][h * 2 + 1]);
+                if (warp == 0 && tig == 0) {
+                    float l = sm.wsum[0][p];
+#pragma unroll
+                    for (int w = 1; w < kWarps; ++w) l += sm.wsum[w][p];
+                    a.pm[idx] = bmax[mt][h];
+                    a.pl[idx] = l;
+                }
+            }
         }
     }
 }
 
+// One CTA per (head, row).  Each thread owns one output dim and folds the blocks
+// in order; loads of later blocks are issued ahead (unrolled) to hide latency.
 __global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const __grid_constant__ AttnDecodeArgs a) {
     __shared__ float wts[1024];
     __shared__ float red[kHeadDim / 32];
@@ -246,11 +309,25 @@ __global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const __grid_const
         __syncthreads();
         for (int b = d; b < n; b += kHeadDim) wts[b] = exp2f(a.pm[base + c + b] - M);
         __syncthreads();
-#pragma unroll 8
-        for (int b = 0; b < n; ++b) {
-            const float w = wts[b];
-            L = fmaf(a.pl[base + c + b], w, L);
-            O = fmaf(a.po[(base + c + b) * kHeadDim + d], w, O);
+        const float* pl = a.pl + base + c;
+        const float* po = a.po + (base + c) * kHeadDim + d;
+        int b = 0;
+        for (; b + 16 <= n; b += 16) {
+            float lv[16], ov[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                lv[u] = pl[b + u];
+                ov[u] = po[(size_t)(b + u) * kHeadDim];
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                L = fmaf(lv[u], wts[b + u], L);
+                O = fmaf(ov[u], wts[b + u], O);
+            }
+        }
+        for (; b < n; ++b) {
+            L = fmaf(pl[b], wts[b], L);
+            O = fmaf(po[(size_t)b * kHeadDim], wts[b], O);
         }
     }
     pdl_trigger();
