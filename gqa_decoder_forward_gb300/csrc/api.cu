@@ -179,6 +179,9 @@ int xbox_index(int rows) {
 }
 constexpr int kXBoxes = 11;
 
+// Row counts up to which the projections after a norm apply the norm themselves.
+constexpr int kMaxFusedNormRows = 8;
+
 }  // namespace
 
 // ---- model / kv objects --------------------------------------------------------
@@ -278,9 +281,15 @@ KvView view(const tfl_kv* kv) {
 // Launches the TMA matvec with weight maps w0..w2 and activation map xm (whose
 // box rows must be matvec_tma_x_rows(e.n_rows)).
 cudaError_t mv_launch(tfl_model* m, const MatvecArgs& e, const CUtensorMap* w0, const CUtensorMap* w1,
-                      const CUtensorMap* w2, const CUtensorMap* xm, cudaStream_t st, bool pdl) {
+                      const CUtensorMap* w2, const CUtensorMap* xm, cudaStream_t st, bool pdl,
+                      const bf16* norm_w = nullptr) {
     MatvecTmaArgs a;
     std::memset(&a, 0, sizeof a);
+    if (norm_w) {  // e.x is the residual stream; the kernel applies the RMSNorm itself
+        a.norm_w = norm_w;
+        a.eps = m->cfg.rms_eps;
+        a.depth = matvec_norm_depth(e.n_rows, e.K);
+    }
     a.e = e;
     a.wmap[0] = *w0;
     if (w1) a.wmap[1] = *w1;
@@ -307,8 +316,11 @@ int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h
         CK(cudaMemcpyAsync(m->h, h_in, (size_t)n * H * 2, cudaMemcpyDeviceToDevice, st));
         LAUNCH(m, K_NORM, st, launch_rmsnorm(m->h, m->attn_norm[0], c.rms_eps, n, H, m->xn, st, false));
     }
+    // up to 8 rows: each projection that follows a norm applies the norm itself
+    const bool fuse = n <= kMaxFusedNormRows;
     for (int l = 0; l < c.layers; ++l) {
-        if (l > 0) LAUNCH(m, K_NORM, st, launch_rmsnorm(m->h, m->attn_norm[l], c.rms_eps, n, H, m->xn, st, pdl));
+        if (l > 0 && !fuse)
+            LAUNCH(m, K_NORM, st, launch_rmsnorm(m->h, m->attn_norm[l], c.rms_eps, n, H, m->xn, st, pdl));
         MatvecArgs a = {};
         a.mode = MV_QKV_ROPE;
         a.K = H;
@@ -327,7 +339,9 @@ int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h
         a.rows = rm;
         const int xi = xbox_index(n);
         const tfl_model::LayerMaps& wm = m->wmaps[l];
-        LAUNCH(m, K_QKV, st, mv_launch(m, a, &wm.q, &wm.k, &wm.v, &m->xmap_xn[xi], st, pdl));
+        if (fuse) a.x = m->h;
+        LAUNCH(m, K_QKV, st,
+               mv_launch(m, a, &wm.q, &wm.k, &wm.v, &m->xmap_xn[xi], st, pdl, fuse ? m->attn_norm[l] : nullptr));
 
         AttnDecodeArgs at = {};
         at.q = m->q;
@@ -353,7 +367,7 @@ int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h
         o.h = m->h;
         LAUNCH(m, K_O, st, mv_launch(m, o, &wm.o, nullptr, nullptr, &m->xmap_ao[xi], st, pdl));
 
-        LAUNCH(m, K_NORM, st, launch_rmsnorm(m->h, m->ffn_norm[l], c.rms_eps, n, H, m->xn, st, pdl));
+        if (!fuse) LAUNCH(m, K_NORM, st, launch_rmsnorm(m->h, m->ffn_norm[l], c.rms_eps, n, H, m->xn, st, pdl));
 
         MatvecArgs gu = {};
         gu.mode = MV_SWIGLU;
@@ -365,7 +379,9 @@ int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h
         gu.n_out = c.ffn;
         gu.y = m->act;
         gu.ldy = c.ffn;
-        LAUNCH(m, K_GATEUP, st, mv_launch(m, gu, &wm.g, &wm.u, nullptr, &m->xmap_xn[xi], st, pdl));
+        if (fuse) gu.x = m->h;
+        LAUNCH(m, K_GATEUP, st,
+               mv_launch(m, gu, &wm.g, &wm.u, nullptr, &m->xmap_xn[xi], st, pdl, fuse ? m->ffn_norm[l] : nullptr));
 
         MatvecArgs d = {};
         d.mode = MV_RESIDUAL;
@@ -384,21 +400,23 @@ int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h
 int run_head(tfl_model* m, int r0, int n, void* logits, long ld_rows_out, cudaStream_t st) {
     const tfl_config& c = m->cfg;
     const int H = c.hidden;
+    const bool pdl = m->pdl && st != nullptr;
     for (int b = 0; b < n; b += kMaxDecodeRows) {
         const int k = std::min(kMaxDecodeRows, n - b);
-        LAUNCH(m, K_NORM, st, launch_rmsnorm(m->h + (size_t)(r0 + b) * H, m->final_norm, c.rms_eps, k, H, m->xn, st,
-                                             m->pdl && st != nullptr));
+        const bool fuse = k <= kMaxFusedNormRows;
+        const bf16* hrows = m->h + (size_t)(r0 + b) * H;
+        if (!fuse) LAUNCH(m, K_NORM, st, launch_rmsnorm(hrows, m->final_norm, c.rms_eps, k, H, m->xn, st, pdl));
         MatvecArgs a = {};
         a.mode = MV_STORE;
         a.K = H;
         a.n_rows = k;
-        a.x = m->xn;
+        a.x = fuse ? hrows : m->xn;
         a.w0 = m->lm_head;
         a.n_out = c.vocab;
         a.y = (bf16*)logits + (size_t)b * ld_rows_out;
         a.ldy = ld_rows_out;
-        LAUNCH(m, K_LMHEAD, st, mv_launch(m, a, &m->lm_map, nullptr, nullptr, &m->xmap_xn[xbox_index(k)], st,
-                                          m->pdl && st != nullptr));
+        LAUNCH(m, K_LMHEAD, st, mv_launch(m, a, &m->lm_map, nullptr, nullptr, &m->xmap_xn[xbox_index(k)], st, pdl,
+                                          fuse ? m->final_norm : nullptr));
     }
     return TFL_OK;
 }
@@ -765,12 +783,13 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
                  void* stream) {
     if (!m || !in || !out) return fail(TFL_E_ARG, "NULL model, in or out");
     const tfl_config& c = m->cfg;
-    if (op < TFL_OP_ATTN_NORM || op > TFL_OP_LM_HEAD) return fail(TFL_E_ARG, "unknown op %d", op);
-    if (op != TFL_OP_FINAL_NORM && op != TFL_OP_LM_HEAD && (layer < 0 || layer >= c.layers))
+    if (op < TFL_OP_ATTN_NORM || op > TFL_OP_NORM_LM_HEAD) return fail(TFL_E_ARG, "unknown op %d", op);
+    const bool no_layer = op == TFL_OP_FINAL_NORM || op == TFL_OP_LM_HEAD || op == TFL_OP_NORM_LM_HEAD;
+    if (!no_layer && (layer < 0 || layer >= c.layers))
         return fail(TFL_E_ARG, "layer %d outside 0..%d", layer, c.layers - 1);
     if (rows < 1 || rows > c.max_decode_rows) return fail(TFL_E_ARG, "rows %d outside 1..%d", rows, c.max_decode_rows);
     if (!aligned16(in) || !aligned16(out)) return fail(TFL_E_ARG, "in/out not 16-byte aligned");
-    const bool uses_kv = op == TFL_OP_QKV_ROPE || op == TFL_OP_ATTENTION;
+    const bool uses_kv = op == TFL_OP_QKV_ROPE || op == TFL_OP_ATTENTION || op == TFL_OP_NORM_QKV_ROPE;
     RowMap rm;
     std::memset(&rm, 0, sizeof rm);
     if (uses_kv) {
@@ -793,6 +812,22 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
     auto xmap = [&](int K) {
         return encode_map(&xm, in, (uint64_t)K, (uint64_t)rows, (uint32_t)matvec_tma_x_rows(rows));
     };
+    // fused norm + projection: in is the residual stream; more than 8 rows run the
+    // norm kernel into the workspace first, then the projection reads it by TMA
+    const bool fused_op = op == TFL_OP_NORM_QKV_ROPE || op == TFL_OP_NORM_GATE_UP || op == TFL_OP_NORM_LM_HEAD;
+    const bf16* norm_w = nullptr;
+    if (fused_op) {
+        const bf16* w = op == TFL_OP_NORM_QKV_ROPE ? m->attn_norm[layer]
+                      : op == TFL_OP_NORM_GATE_UP ? m->ffn_norm[layer] : m->final_norm;
+        if (rows <= kMaxFusedNormRows) {
+            norm_w = w;
+        } else {
+            LAUNCH(m, K_NORM, st, launch_rmsnorm((const bf16*)in, w, c.rms_eps, rows, H, m->xn, st, false));
+            a.x = m->xn;
+            in = m->xn;
+        }
+        op = op == TFL_OP_NORM_QKV_ROPE ? TFL_OP_QKV_ROPE : op == TFL_OP_NORM_GATE_UP ? TFL_OP_GATE_UP : TFL_OP_LM_HEAD;
+    }
     switch (op) {
         case TFL_OP_ATTN_NORM:
         case TFL_OP_FFN_NORM:
@@ -818,7 +853,8 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.rows = rm;
             if (!xmap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
             LAUNCH(m, K_QKV, st,
-                   mv_launch(m, a, &m->wmaps[layer].q, &m->wmaps[layer].k, &m->wmaps[layer].v, &xm, st, false));
+                   mv_launch(m, a, &m->wmaps[layer].q, &m->wmaps[layer].k, &m->wmaps[layer].v, &xm, st, false,
+                             norm_w));
             break;
         case TFL_OP_ATTENTION: {
             AttnDecodeArgs at = {};
@@ -858,7 +894,7 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.ldy = c.ffn;
             if (!xmap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
             LAUNCH(m, K_GATEUP, st,
-                   mv_launch(m, a, &m->wmaps[layer].g, &m->wmaps[layer].u, nullptr, &xm, st, false));
+                   mv_launch(m, a, &m->wmaps[layer].g, &m->wmaps[layer].u, nullptr, &xm, st, false, norm_w));
             break;
         case TFL_OP_LM_HEAD:
             a.mode = MV_STORE;
@@ -868,7 +904,7 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.y = (bf16*)out;
             a.ldy = c.vocab;
             if (!xmap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
-            LAUNCH(m, K_LMHEAD, st, mv_launch(m, a, &m->lm_map, nullptr, nullptr, &xm, st, false));
+            LAUNCH(m, K_LMHEAD, st, mv_launch(m, a, &m->lm_map, nullptr, nullptr, &xm, st, false, norm_w));
             break;
     }
     return ok();

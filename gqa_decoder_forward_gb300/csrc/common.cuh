@@ -98,11 +98,17 @@ struct MatvecTmaArgs {
     int tiles;              // tiles of 16 weight rows
     int kstages;            // ceil(K / 512)
     int* status;
+    // fused RMSNorm (up to 8 rows, K = hidden): e.x is the residual stream and
+    // the kernel normalises it with norm_w; xmap is unused
+    const bf16* norm_w;
+    float eps;
+    int depth;              // ring stages of the fused-norm variant (matvec_norm_depth)
 };
 int matvec_tma_nt(int n_rows);
 int matvec_tma_x_rows(int n_rows);
 int matvec_tma_tiles(const MatvecArgs& e);
 cudaError_t init_matvec_tma();
+int matvec_norm_depth(int n_rows, int K);
 cudaError_t launch_matvec_tma(const MatvecTmaArgs& a, int grid, cudaStream_t st, bool pdl);
 
 cudaError_t launch_embed_rmsnorm(const int32_t* ids, const bf16* embed, int vocab, const bf16* w, float eps,

@@ -28,6 +28,7 @@
 
 #include "common.cuh"
 #include "matvec_epilogue.cuh"
+#include "rmsnorm_row.cuh"
 #include "tma.cuh"
 
 namespace tfl {
@@ -45,6 +46,21 @@ struct Cfg {
     static constexpr int kDepth = (200 * 1024 / kStage) < 8 ? (200 * 1024 / kStage) : 8;
     static constexpr int kRed = kConsumerWarps * NT * 4 * 32 * 4;  // cross-warp sums
     static constexpr int kSmem = 1024 + kDepth * kStage + kRed + 2 * kDepth * 8 + 64;
+};
+
+// Fused-norm variant (up to 8 activation rows): stages hold weights only; the
+// normalised rows live in shared memory for the whole kernel.
+struct NormCfg {
+    static constexpr int kBudget = 216 * 1024;
+    static constexpr int kRed = kConsumerWarps * 4 * 32 * 4;
+    static constexpr int kRedNorm = 8 * 8 * 4;
+    static int depth(int xn_bytes) {
+        int d = (kBudget - 1024 - xn_bytes - kRed - kRedNorm - 2 * 8 * 8 - 64) / kABytes;
+        return d < 8 ? d : 8;
+    }
+    static int smem(int depth, int xn_bytes) {
+        return 1024 + depth * kABytes + xn_bytes + kRed + kRedNorm + 2 * 8 * 8 + 64;
+    }
 };
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -117,23 +133,30 @@ __device__ __forceinline__ void load_weights(const MatvecTmaArgs& a, int t, int 
     }
 }
 
-template <int NT>
+// NORM: the activation rows are the residual stream a.e.x and are normalised
+// (with a.norm_w) into shared memory by the consumers; requires NT == 1.
+template <int NT, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_constant__ MatvecTmaArgs a) {
     using C = Cfg<NT>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* red = reinterpret_cast<float*>(base + C::kDepth * C::kStage);
-    uint64_t* full = reinterpret_cast<uint64_t*>(base + C::kDepth * C::kStage + C::kRed);
-    uint64_t* empty = full + C::kDepth;
-    volatile int* s_abort = reinterpret_cast<volatile int*>(empty + C::kDepth);
+    const int depth = NORM ? a.depth : C::kDepth;
+    const int stage_bytes = NORM ? kABytes : C::kStage;
+    const int xn_bytes = NORM ? a.e.n_rows * a.e.K * 2 : 0;
+    unsigned char* xn = base + depth * stage_bytes;  // NORM: [k-block][row][64], swizzled lines
+    float* red = reinterpret_cast<float*>(xn + xn_bytes);
+    float* red_norm = red + kConsumerWarps * NT * 4 * 32;
+    uint64_t* full = reinterpret_cast<uint64_t*>(red_norm + (NORM ? 64 : 0));
+    uint64_t* empty = full + depth;
+    volatile int* s_abort = reinterpret_cast<volatile int*>(empty + depth);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles = a.tiles, nst = a.kstages;
-    // stage bytes actually moved: weights + x rows present in the box
-    const uint32_t stage_tx = kABytes + a.x_rows_box * 128 * kKbPerStage;
+    // stage bytes actually moved: weights (+ x rows present in the box)
+    const uint32_t stage_tx = kABytes + (NORM ? 0 : a.x_rows_box * 128 * kKbPerStage);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kDepth; ++s) {
+        for (int s = 0; s < depth; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
@@ -149,29 +172,30 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
             int t = blockIdx.x, ks = 0;
             // weight stages that fit the ring are issued before waiting for the
             // kernels that produce the activations
-            int pre_ks[C::kDepth];
+            int pre_ks[8];
             int n_pre = 0;
-            while (n_pre < C::kDepth && t < tiles) {
+            while (n_pre < depth && t < tiles) {
                 mbar_arrive_expect_tx(&full[n_pre], stage_tx);
-                load_weights(a, t, ks * kKbPerStage, base + n_pre * C::kStage, &full[n_pre], pw);
+                load_weights(a, t, ks * kKbPerStage, base + n_pre * stage_bytes, &full[n_pre], pw);
                 pre_ks[n_pre++] = ks;
                 if (++ks == nst) { ks = 0; t += gridDim.x; }
             }
             pdl_wait();
-            for (int i = 0; i < n_pre; ++i)
-                tma_load_3d(base + i * C::kStage + kABytes, &a.xmap, 0, 0, pre_ks[i] * kKbPerStage, &full[i], px);
-            int stage = n_pre % C::kDepth;
-            uint32_t phase = n_pre == C::kDepth ? 1u : 0u;
+            if (!NORM)
+                for (int i = 0; i < n_pre; ++i)
+                    tma_load_3d(base + i * stage_bytes + kABytes, &a.xmap, 0, 0, pre_ks[i] * kKbPerStage, &full[i], px);
+            int stage = n_pre % depth;
+            uint32_t phase = n_pre == depth ? 1u : 0u;
             while (t < tiles) {
                 if (*s_abort || !mbar_wait(&empty[stage], phase ^ 1u, a.status)) {
                     *s_abort = 1;
                     break;
                 }
-                unsigned char* sA = base + stage * C::kStage;
+                unsigned char* sA = base + stage * stage_bytes;
                 mbar_arrive_expect_tx(&full[stage], stage_tx);
                 load_weights(a, t, ks * kKbPerStage, sA, &full[stage], pw);
-                tma_load_3d(sA + kABytes, &a.xmap, 0, 0, ks * kKbPerStage, &full[stage], px);
-                if (++stage == C::kDepth) { stage = 0; phase ^= 1u; }
+                if (!NORM) tma_load_3d(sA + kABytes, &a.xmap, 0, 0, ks * kKbPerStage, &full[stage], px);
+                if (++stage == depth) { stage = 0; phase ^= 1u; }
                 if (++ks == nst) { ks = 0; t += gridDim.x; }
             }
             // after an abort, give copies already issued time to land before exiting
@@ -187,6 +211,32 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
     const int g = lane >> 2, tig = lane & 3;
     const int R = a.e.n_rows, xrows = a.x_rows_box;
     const uint32_t base_u = smem_u32(base);
+    const uint32_t xn_u = smem_u32(xn);
+    const int kblocks = a.e.K / 64;
+    if (NORM) {
+        // the rows' RMSNorm, with the same arithmetic as the standalone norm kernel,
+        // into [k-block][row][64] lines (chunk c of line l at c ^ (l mod 8))
+        const int K = a.e.K, tid = threadIdx.x;
+        for (int r = 0; r < R; ++r) {
+            const bf16* hr = a.e.x + (size_t)r * K;
+            const float rinv = rms_inv(hr, K, a.eps, tid, red_norm + r * 8, [] { named_barrier(1, kConsumerWarps * 32); });
+            for (int i = tid * 8; i < K; i += kNormThreads * 8) {
+                const uint4 hv = *reinterpret_cast<const uint4*>(hr + i);
+                const uint4 wv = __ldg(reinterpret_cast<const uint4*>(a.norm_w + i));
+                const bf16* he = reinterpret_cast<const bf16*>(&hv);
+                const bf16* we = reinterpret_cast<const bf16*>(&wv);
+                uint4 o;
+                bf16* oe = reinterpret_cast<bf16*>(&o);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) oe[k] = rms_apply(he[k], we[k], rinv);
+                const int line = (i >> 6) * R + r, c = (i & 63) >> 3;
+                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xn_u + line * 128 + ((c ^ (line & 7)) << 4)),
+                             "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
+                             : "memory");
+            }
+        }
+        named_barrier(1, kConsumerWarps * 32);
+    }
     // line of this warp's lo / hi weight row inside a stage: [k-block][16 rows]
     // for STORE/RESIDUAL; [k-block][8 lo rows] then [k-block][8 hi rows] otherwise
     const bool two_boxes = a.e.mode == MV_SWIGLU || a.e.mode == MV_QKV_ROPE;
@@ -202,8 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
             // after an abort every consumer keeps walking the loops (no more waits,
             // no early return) so that all of them reach the named barriers below
             if (!*s_abort && !mbar_wait(&full[stage], phase, a.status)) *s_abort = 1;
-            const uint32_t sA = base_u + stage * C::kStage;
+            const uint32_t sA = base_u + stage * stage_bytes;
             const uint32_t sX = sA + kABytes;
+            const int kb = ks * kKbPerStage + warp;  // this warp's k-block
             uint4 l0, l1, h0, h1;
             line_chunks(sA, line_lo, tig, l0, l1);
             line_chunks(sA, line_hi, tig, h0, h1);
@@ -211,7 +262,11 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
             for (int n = 0; n < NT; ++n) {
                 const int xr = n * 8 + g;  // activation row of this lane's B fragment
                 uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
-                if (xr < xrows) line_chunks(sX, warp * xrows + xr, tig, x0, x1);
+                if (NORM) {
+                    if (xr < R && kb < kblocks) line_chunks(xn_u, kb * R + xr, tig, x0, x1);
+                } else if (xr < xrows) {
+                    line_chunks(sX, warp * xrows + xr, tig, x0, x1);
+                }
                 mma16816(acc[n], l0.x, h0.x, l0.y, h0.y, x0.x, x0.y);
                 mma16816(acc[n], l0.z, h0.z, l0.w, h0.w, x0.z, x0.w);
                 mma16816(acc[n], l1.x, h1.x, l1.y, h1.y, x1.x, x1.y);
@@ -219,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == C::kDepth) { stage = 0; phase ^= 1u; }
+            if (++stage == depth) { stage = 0; phase ^= 1u; }
         }
         // fixed-order sum over the eight warps, then the epilogue
 #pragma unroll
@@ -247,19 +302,19 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
     pdl_trigger();
 }
 
-template <int NT>
+template <int NT, bool NORM>
 cudaError_t launch_nt(const MatvecTmaArgs& a, int grid, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<NT>::kSmem;
+    cfg.dynamicSmemBytes = NORM ? NormCfg::smem(a.depth, a.e.n_rows * a.e.K * 2) : Cfg<NT>::kSmem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, matvec_tma_kernel<NT>, a);
+    return cudaLaunchKernelEx(&cfg, matvec_tma_kernel<NT, NORM>, a);
 }
 
 }  // namespace
@@ -276,14 +331,19 @@ int matvec_tma_tiles(const MatvecArgs& e) {
 
 cudaError_t init_matvec_tma() {
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   Cfg<1>::kSmem)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   Cfg<2>::kSmem)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   Cfg<4>::kSmem)) != cudaSuccess) return e;
-    return cudaFuncSetAttribute(matvec_tma_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<8>::kSmem);
+    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  Cfg<8>::kSmem)) != cudaSuccess) return e;
+    return cudaFuncSetAttribute(matvec_tma_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                NormCfg::kBudget);
 }
+
+int matvec_norm_depth(int n_rows, int K) { return NormCfg::depth(n_rows * K * 2); }
 
 cudaError_t launch_matvec_tma(const MatvecTmaArgs& a, int grid, cudaStream_t st, bool pdl) {
     const int nt = matvec_tma_nt(a.e.n_rows);
@@ -292,11 +352,17 @@ cudaError_t launch_matvec_tma(const MatvecTmaArgs& a, int grid, cudaStream_t st,
         a.kstages != (a.e.K + 64 * kKbPerStage - 1) / (64 * kKbPerStage))
         return cudaErrorInvalidValue;
     if (grid > a.tiles) grid = a.tiles;
+    if (a.norm_w) {
+        if (nt != 1 || a.depth < 2 || a.depth > 8 || a.depth != NormCfg::depth(a.e.n_rows * a.e.K * 2) ||
+            a.e.K % 64 != 0)
+            return cudaErrorInvalidValue;
+        return launch_nt<1, true>(a, grid, st, pdl);
+    }
     switch (nt) {
-        case 1: return launch_nt<1>(a, grid, st, pdl);
-        case 2: return launch_nt<2>(a, grid, st, pdl);
-        case 4: return launch_nt<4>(a, grid, st, pdl);
-        default: return launch_nt<8>(a, grid, st, pdl);
+        case 1: return launch_nt<1, false>(a, grid, st, pdl);
+        case 2: return launch_nt<2, false>(a, grid, st, pdl);
+        case 4: return launch_nt<4, false>(a, grid, st, pdl);
+        default: return launch_nt<8, false>(a, grid, st, pdl);
     }
 }
 

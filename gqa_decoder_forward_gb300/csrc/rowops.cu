@@ -12,37 +12,14 @@
 // largest logit, the lowest id among equal maxima; a row with any non-finite
 // logit yields -1 and raises a bit of the device status word.
 #include "common.cuh"
+#include "rmsnorm_row.cuh"
 
 namespace tfl {
 namespace {
 
-constexpr int kNormThreads = 256;
-
-__device__ __forceinline__ float block_sum_fixed(float v, float* red) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    if ((threadIdx.x & 31) == 0) red[warp] = v;
-    __syncthreads();
-    float s = red[0];
-    for (int w = 1; w < nw; ++w) s += red[w];
-    return s;
-}
-
 // x: the row (H bf16, 16-byte aligned); writes the normalised row to out.
 __device__ __forceinline__ void rmsnorm_row(const bf16* x, const bf16* w, float eps, int H, bf16* out, float* red) {
-    float ss = 0.f;
-    for (int i = threadIdx.x * 8; i < H; i += kNormThreads * 8) {
-        uint4 v = *reinterpret_cast<const uint4*>(x + i);
-        const bf16* e = reinterpret_cast<const bf16*>(&v);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            float f = bf(e[k]);
-            ss = fmaf(f, f, ss);
-        }
-    }
-    ss = block_sum_fixed(ss, red);
-    const float r = 1.0f / sqrtf(ss / (float)H + eps);
+    const float r = rms_inv(x, H, eps, threadIdx.x, red, [] { __syncthreads(); });
     for (int i = threadIdx.x * 8; i < H; i += kNormThreads * 8) {
         uint4 v = *reinterpret_cast<const uint4*>(x + i);
         uint4 wv = __ldg(reinterpret_cast<const uint4*>(w + i));
@@ -51,7 +28,7 @@ __device__ __forceinline__ void rmsnorm_row(const bf16* x, const bf16* w, float 
         uint4 o;
         bf16* oe = reinterpret_cast<bf16*>(&o);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) oe[k] = rn(bf(we[k]) * rbf(bf(e[k]) * r));
+        for (int k = 0; k < 8; ++k) oe[k] = rms_apply(e[k], we[k], r);
         *reinterpret_cast<uint4*>(out + i) = o;
     }
 }

@@ -282,7 +282,8 @@ def tfl_status(model: Model, stream=None) -> int:
 
 
 OPS = {"attn_norm": 0, "qkv_rope": 1, "attention": 2, "o_residual": 3, "ffn_norm": 4, "gate_up": 5,
-       "down_residual": 6, "final_norm": 7, "lm_head": 8}
+       "down_residual": 6, "final_norm": 7, "lm_head": 8, "norm_qkv_rope": 9, "norm_gate_up": 10,
+       "norm_lm_head": 11}
 
 
 def tfl_layer_op(model: Model, op: str, layer: int, inp: torch.Tensor, out: torch.Tensor, kv: "KV" = None,

@@ -253,6 +253,10 @@ int tfl_head(tfl_model* model, const void* h, int rows, void* logits, void* stre
  *   TFL_OP_DOWN_RESIDUAL in act [rows][F]; out h updated: h = bf16(h + bf16(Wd[layer] . in))
  *   TFL_OP_FINAL_NORM    in h -> out RMSNorm with final_norm (layer ignored)
  *   TFL_OP_LM_HEAD       in xn [rows][H] -> out logits [rows][V] (layer ignored)
+ *   TFL_OP_NORM_QKV_ROPE, TFL_OP_NORM_GATE_UP, TFL_OP_NORM_LM_HEAD: the norm and
+ *                        the projection after it in one op, as a decode step
+ *                        runs them: in is the residual stream h; the result is
+ *                        bit-identical to the norm op followed by the projection op
  * Buffers are 16-byte aligned; in and out must not overlap.
  */
 #define TFL_OP_ATTN_NORM 0
@@ -264,6 +268,9 @@ int tfl_head(tfl_model* model, const void* h, int rows, void* logits, void* stre
 #define TFL_OP_DOWN_RESIDUAL 6
 #define TFL_OP_FINAL_NORM 7
 #define TFL_OP_LM_HEAD 8
+#define TFL_OP_NORM_QKV_ROPE 9
+#define TFL_OP_NORM_GATE_UP 10
+#define TFL_OP_NORM_LM_HEAD 11
 int tfl_layer_op(tfl_model* model, int op, int layer, tfl_kv* kv, int pos0, int rows, const void* in, void* out,
                  void* stream);
 

@@ -350,3 +350,39 @@ def test_long_ragged_context_tiny(orc, tiny):
     got = synth.bits(lg3)
     assert np.abs(gu.bf16_to_f64(got) - gu.bf16_to_f64(ref[1000:])).max() <= 0.05
     assert gu.kl_mean(ref[1000:], got) <= 1e-4
+
+
+@pytest.mark.parametrize("R", [1, 3, 8, 16])
+def test_fused_norm_ops_equal_norm_then_projection(tiny, R):
+    """The decode path applies the RMSNorm inside the projection that follows it
+    (up to 8 rows); that must give exactly the norm op followed by the projection op."""
+    w, _ = tiny
+    m = _tiny_model(w, max_context=512)
+    H, F, V = TINY.hidden, TINY.ffn, TINY.vocab
+    h = synth.normal_bf16(81, 0, (R, H), 0.7, "cuda")
+    for layer in range(TINY.layers):
+        kv_a, kv_b = m.kv(512), m.kv(512)
+        xn = torch.empty_like(h)
+        tfl.tfl_layer_op(m, "attn_norm", layer, h, xn)
+        q_ref = torch.empty((R, TINY.n_q * 128), dtype=torch.bfloat16, device="cuda")
+        tfl.tfl_layer_op(m, "qkv_rope", layer, xn, q_ref, kv_a, 100)
+        q = torch.empty_like(q_ref)
+        tfl.tfl_layer_op(m, "norm_qkv_rope", layer, h, q, kv_b, 100)
+        assert torch.equal(q.view(torch.int16), q_ref.view(torch.int16))
+        ka, va = kv_a.read(layer, 100, R)
+        kb, vb = kv_b.read(layer, 100, R)
+        assert torch.equal(ka.view(torch.int16), kb.view(torch.int16))
+        assert torch.equal(va.view(torch.int16), vb.view(torch.int16))
+
+        tfl.tfl_layer_op(m, "ffn_norm", layer, h, xn)
+        a_ref = torch.empty((R, F), dtype=torch.bfloat16, device="cuda")
+        tfl.tfl_layer_op(m, "gate_up", layer, xn, a_ref)
+        a = torch.empty_like(a_ref)
+        tfl.tfl_layer_op(m, "norm_gate_up", layer, h, a)
+        assert torch.equal(a.view(torch.int16), a_ref.view(torch.int16))
+    tfl.tfl_layer_op(m, "final_norm", 0, h, xn)
+    l_ref = torch.empty((R, V), dtype=torch.bfloat16, device="cuda")
+    tfl.tfl_layer_op(m, "lm_head", 0, xn, l_ref)
+    lg = torch.empty_like(l_ref)
+    tfl.tfl_layer_op(m, "norm_lm_head", 0, h, lg)
+    assert torch.equal(lg.view(torch.int16), l_ref.view(torch.int16))
