@@ -171,6 +171,21 @@ bool encode_map(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, uint
     return r == CUDA_SUCCESS;
 }
 
+// A 2-D bf16 tensor map over a row-major [rows][K] matrix with 128-byte
+// swizzle and boxes of (64 columns, box_rows rows): the GEMM operands.
+bool encode_map2d(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn || ((uintptr_t)ptr & 15u) || K % 64 != 0 || box_rows < 1 || box_rows > 256) return false;
+    cuuint64_t dims[2] = {K, rows};
+    cuuint64_t strides[1] = {K * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Index of the activation-row box for a call of `rows` rows: 1..8 -> 0..7,
 // 16 -> 8, 32 -> 9, 64 -> 10.
 int xbox_index(int rows) {
@@ -209,11 +224,13 @@ struct tfl_model {
     bool pdl;
     // TMA descriptors of every projection and of the activation buffers
     struct LayerMaps {
-        CUtensorMap q, k, v, o, g, u, d;
+        CUtensorMap q, k, v, o, g, u, d;                // decode matvec (3-D)
+        CUtensorMap gq, gk, gv, go, gg, gu, gd;         // prompt GEMM (2-D)
     };
     std::vector<LayerMaps> wmaps;
     CUtensorMap lm_map;
     CUtensorMap xmap_xn[kXBoxes], xmap_ao[kXBoxes], xmap_act[kXBoxes];  // by xbox_index(rows)
+    CUtensorMap amap_xn, amap_ao, amap_act;  // GEMM activation operands (128-row boxes)
     int grid = 0;
     bool prof = false;
     std::vector<Mark> marks;         // recorded while profiling
@@ -468,9 +485,114 @@ int decode_common(tfl_model* m, tfl_kv* const* kvs, int n_streams, const int* ro
     return ok();
 }
 
-// A prompt chunk runs as consecutive windows of <= max_decode_rows rows
-// through the decode kernels: each row's result is independent of the window
-// it falls in, so chunk boundaries never change results.
+// Launches the prompt GEMM for one projection (tiles derived from the mode).
+cudaError_t gemm_launch(tfl_model* m, const MatvecArgs& e, const CUtensorMap* amap, const CUtensorMap* b0,
+                        const CUtensorMap* b1, const CUtensorMap* b2, cudaStream_t st, bool pdl) {
+    GemmArgs g;
+    std::memset(&g, 0, sizeof g);
+    g.e = e;
+    g.amap = *amap;
+    g.bmap[0] = *b0;
+    if (b1) g.bmap[1] = *b1;
+    if (b2) g.bmap[2] = *b2;
+    g.m_tiles = (e.n_rows + 127) / 128;
+    g.n_tiles = e.mode == MV_SWIGLU ? e.n_out / 64 : e.mode == MV_QKV_ROPE ? e.n_q + 2 * e.n_kv : e.n_out / 256;
+    g.kblocks = e.K / 64;
+    g.status = m->status;
+    return launch_gemm_tc(g, m->grid, st, pdl);
+}
+
+// Attention of the rows of a prompt chunk (one stream, queries q, output out,
+// both [rows][n_q*128]) through the decode attention kernels, in windows of
+// max_decode_rows rows; each row's result is independent of the windowing.
+int prompt_attention(tfl_model* m, const RowMap& rm, int layer, const bf16* q, bf16* out, cudaStream_t st,
+                     bool pdl) {
+    const tfl_config& c = m->cfg;
+    const int qd = c.n_q * kHeadDim;
+    for (int w0 = 0; w0 < rm.n_rows; w0 += c.max_decode_rows) {
+        const int k = std::min(c.max_decode_rows, rm.n_rows - w0);
+        AttnDecodeArgs at = {};
+        at.q = q + (size_t)w0 * qd;
+        at.out = out + (size_t)w0 * qd;
+        at.pm = m->pm;
+        at.pl = m->pl;
+        at.po = m->po;
+        at.max_blocks = m->L.max_blocks;
+        at.n_q = c.n_q;
+        at.n_kv = c.n_kv;
+        at.layer = layer;
+        at.rows.n_streams = 1;
+        at.rows.n_rows = k;
+        at.rows.row_start[1] = k;
+        at.rows.pos0[0] = rm.pos0[0] + w0;
+        at.rows.kv[0] = rm.kv[0];
+        LAUNCH(m, K_ATTN, st, launch_attn_block(at, st, pdl));
+        LAUNCH(m, K_MERGE, st, launch_attn_merge(at, st, pdl));
+    }
+    return TFL_OK;
+}
+
+// The layer stack over the n rows of one prompt chunk (one stream): norms,
+// tcgen05 GEMM projections with fused epilogues, attention.  Each row's result
+// depends only on its own input and position, so chunk boundaries never change
+// results (a prompt resumed from a kept prefix equals the same prompt fresh).
+int run_prompt_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h_in, cudaStream_t st) {
+    const tfl_config& c = m->cfg;
+    const int n = rm.n_rows, H = c.hidden, qd = c.n_q * kHeadDim;
+    const bool pdl = m->pdl && st != nullptr;
+    if (ids) {
+        LAUNCH(m, K_EMBED, st,
+               launch_embed_rmsnorm(ids, m->embed, c.vocab, m->attn_norm[0], c.rms_eps, n, H, m->h, m->xn, m->status,
+                                    st, pdl));
+    } else {
+        CK(cudaMemcpyAsync(m->h, h_in, (size_t)n * H * 2, cudaMemcpyDeviceToDevice, st));
+        LAUNCH(m, K_NORM, st, launch_rmsnorm(m->h, m->attn_norm[0], c.rms_eps, n, H, m->xn, st, false));
+    }
+    for (int l = 0; l < c.layers; ++l) {
+        const tfl_model::LayerMaps& wm = m->wmaps[l];
+        if (l > 0) LAUNCH(m, K_NORM, st, launch_rmsnorm(m->h, m->attn_norm[l], c.rms_eps, n, H, m->xn, st, pdl));
+        MatvecArgs a = {};
+        a.mode = MV_QKV_ROPE;
+        a.K = H;
+        a.n_rows = n;
+        a.n_q = c.n_q;
+        a.n_kv = c.n_kv;
+        a.y = m->q;
+        a.ldy = qd;
+        a.cos_t = m->cos_t;
+        a.sin_t = m->sin_t;
+        a.layer = l;
+        a.rows = rm;
+        LAUNCH(m, K_QKV, st, gemm_launch(m, a, &m->amap_xn, &wm.gq, &wm.gk, &wm.gv, st, pdl));
+        int e = prompt_attention(m, rm, l, m->q, m->ao, st, pdl);
+        if (e) return e;
+        MatvecArgs o = {};
+        o.mode = MV_RESIDUAL;
+        o.K = qd;
+        o.n_rows = n;
+        o.n_out = H;
+        o.h = m->h;
+        LAUNCH(m, K_O, st, gemm_launch(m, o, &m->amap_ao, &wm.go, nullptr, nullptr, st, pdl));
+        LAUNCH(m, K_NORM, st, launch_rmsnorm(m->h, m->ffn_norm[l], c.rms_eps, n, H, m->xn, st, pdl));
+        MatvecArgs gu = {};
+        gu.mode = MV_SWIGLU;
+        gu.K = H;
+        gu.n_rows = n;
+        gu.n_out = c.ffn;
+        gu.y = m->act;
+        gu.ldy = c.ffn;
+        LAUNCH(m, K_GATEUP, st, gemm_launch(m, gu, &m->amap_xn, &wm.gg, &wm.gu, nullptr, st, pdl));
+        MatvecArgs d = {};
+        d.mode = MV_RESIDUAL;
+        d.K = c.ffn;
+        d.n_rows = n;
+        d.n_out = H;
+        d.h = m->h;
+        LAUNCH(m, K_DOWN, st, gemm_launch(m, d, &m->amap_act, &wm.gd, nullptr, nullptr, st, pdl));
+    }
+    return TFL_OK;
+}
+
 int prefill_common(tfl_model* m, tfl_kv* kv, const int32_t* ids, const void* h_in, int n_rows, void* logits,
                    int all_rows, void* h_out, cudaStream_t st) {
     if (!m || !kv || kv->model != m) return fail(TFL_E_ARG, "NULL model or KV object of another model");
@@ -479,27 +601,22 @@ int prefill_common(tfl_model* m, tfl_kv* kv, const int32_t* ids, const void* h_i
         return fail(TFL_E_CAPACITY, "positions %d..%d reach the KV capacity %d; rejected", kv->length,
                     kv->length + n_rows - 1, std::min(kv->max_pos, m->cfg.max_context));
     const int H = m->cfg.hidden;
-    const int win = m->cfg.max_decode_rows;
-    for (int r = 0; r < n_rows; r += win) {
-        const int k = std::min(win, n_rows - r);
-        RowMap rm;
-        std::memset(&rm, 0, sizeof rm);
-        rm.n_streams = 1;
-        rm.n_rows = k;
-        rm.row_start[1] = k;
-        rm.pos0[0] = kv->length + r;
-        rm.kv[0] = view(kv);
-        int e = run_layers(m, rm, ids ? ids + r : nullptr, h_in ? (const char*)h_in + (size_t)r * H * 2 : nullptr, st);
+    RowMap rm;
+    std::memset(&rm, 0, sizeof rm);
+    rm.n_streams = 1;
+    rm.n_rows = n_rows;
+    rm.row_start[1] = n_rows;
+    rm.pos0[0] = kv->length;
+    rm.kv[0] = view(kv);
+    int e = run_prompt_layers(m, rm, ids, h_in, st);
+    if (e) return e;
+    if (h_out) CK(cudaMemcpyAsync(h_out, m->h, (size_t)n_rows * H * 2, cudaMemcpyDeviceToDevice, st));
+    if (logits && all_rows) {
+        e = run_head(m, 0, n_rows, logits, m->cfg.vocab, st);
         if (e) return e;
-        if (h_out) CK(cudaMemcpyAsync((char*)h_out + (size_t)r * H * 2, m->h, (size_t)k * H * 2,
-                                      cudaMemcpyDeviceToDevice, st));
-        if (logits && all_rows) {
-            e = run_head(m, 0, k, (bf16*)logits + (size_t)r * m->cfg.vocab, m->cfg.vocab, st);
-            if (e) return e;
-        } else if (logits && r + k == n_rows) {
-            e = run_head(m, k - 1, 1, logits, m->cfg.vocab, st);
-            if (e) return e;
-        }
+    } else if (logits) {
+        e = run_head(m, n_rows - 1, 1, logits, m->cfg.vocab, st);
+        if (e) return e;
     }
     kv->length += n_rows;
     return ok();
@@ -638,7 +755,11 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
             okm = encode_map(&x.q, m->wq[l], H, QD, 8) && encode_map(&x.k, m->wk[l], H, KD, 8) &&
                   encode_map(&x.v, m->wv[l], H, KD, 8) && encode_map(&x.o, m->wo[l], QD, H, 16) &&
                   encode_map(&x.g, m->wg[l], H, F, 8) && encode_map(&x.u, m->wu[l], H, F, 8) &&
-                  encode_map(&x.d, m->wd[l], F, H, 16);
+                  encode_map(&x.d, m->wd[l], F, H, 16) &&
+                  encode_map2d(&x.gq, m->wq[l], H, QD, 128) && encode_map2d(&x.gk, m->wk[l], H, KD, 128) &&
+                  encode_map2d(&x.gv, m->wv[l], H, KD, 128) && encode_map2d(&x.go, m->wo[l], QD, H, 256) &&
+                  encode_map2d(&x.gg, m->wg[l], H, F, 64) && encode_map2d(&x.gu, m->wu[l], H, F, 64) &&
+                  encode_map2d(&x.gd, m->wd[l], F, H, 256);
         }
         okm = okm && encode_map(&m->lm_map, m->lm_head, H, cfg->vocab, 16);
         const int xrows[kXBoxes] = {1, 2, 3, 4, 5, 6, 7, 8, 16, 32, 64};
@@ -646,8 +767,11 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
             okm = encode_map(&m->xmap_xn[i], m->xn, H, rows, xrows[i]) &&
                   encode_map(&m->xmap_ao[i], m->ao, QD, rows, xrows[i]) &&
                   encode_map(&m->xmap_act[i], m->act, F, rows, xrows[i]);
+        okm = okm && encode_map2d(&m->amap_xn, m->xn, H, rows, 128) && encode_map2d(&m->amap_ao, m->ao, QD, rows, 128) &&
+              encode_map2d(&m->amap_act, m->act, F, rows, 128);
         cudaError_t ce0 = cudaSuccess;
         if (okm) ce0 = init_matvec_tma();
+        if (okm && ce0 == cudaSuccess) ce0 = init_gemm_tc();
         if (!okm || ce0 != cudaSuccess) {
             delete m;
             return fail(TFL_E_CUDA, "building TMA descriptors failed%s%s", ce0 ? ": " : "",
@@ -783,11 +907,16 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
                  void* stream) {
     if (!m || !in || !out) return fail(TFL_E_ARG, "NULL model, in or out");
     const tfl_config& c = m->cfg;
+    const bool prompt = (op & TFL_OP_PROMPT) != 0;
+    op &= ~TFL_OP_PROMPT;
     if (op < TFL_OP_ATTN_NORM || op > TFL_OP_NORM_LM_HEAD) return fail(TFL_E_ARG, "unknown op %d", op);
     const bool no_layer = op == TFL_OP_FINAL_NORM || op == TFL_OP_LM_HEAD || op == TFL_OP_NORM_LM_HEAD;
     if (!no_layer && (layer < 0 || layer >= c.layers))
         return fail(TFL_E_ARG, "layer %d outside 0..%d", layer, c.layers - 1);
-    if (rows < 1 || rows > c.max_decode_rows) return fail(TFL_E_ARG, "rows %d outside 1..%d", rows, c.max_decode_rows);
+    if (prompt && (op == TFL_OP_LM_HEAD || op == TFL_OP_NORM_LM_HEAD))
+        return fail(TFL_E_ARG, "the prompt path computes logits with the decode head; run op %d without TFL_OP_PROMPT", op);
+    const int max_r = prompt ? c.max_rows : c.max_decode_rows;
+    if (rows < 1 || rows > max_r) return fail(TFL_E_ARG, "rows %d outside 1..%d", rows, max_r);
     if (!aligned16(in) || !aligned16(out)) return fail(TFL_E_ARG, "in/out not 16-byte aligned");
     const bool uses_kv = op == TFL_OP_QKV_ROPE || op == TFL_OP_ATTENTION || op == TFL_OP_NORM_QKV_ROPE;
     RowMap rm;
@@ -812,6 +941,8 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
     auto xmap = [&](int K) {
         return encode_map(&xm, in, (uint64_t)K, (uint64_t)rows, (uint32_t)matvec_tma_x_rows(rows));
     };
+    // ... or as the A operand of the prompt GEMM (128-row boxes)
+    auto amap = [&](int K) { return encode_map2d(&xm, in, (uint64_t)K, (uint64_t)rows, 128); };
     // fused norm + projection: in is the residual stream; more than 8 rows run the
     // norm kernel into the workspace first, then the projection reads it by TMA
     const bool fused_op = op == TFL_OP_NORM_QKV_ROPE || op == TFL_OP_NORM_GATE_UP || op == TFL_OP_NORM_LM_HEAD;
@@ -819,7 +950,7 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
     if (fused_op) {
         const bf16* w = op == TFL_OP_NORM_QKV_ROPE ? m->attn_norm[layer]
                       : op == TFL_OP_NORM_GATE_UP ? m->ffn_norm[layer] : m->final_norm;
-        if (rows <= kMaxFusedNormRows) {
+        if (rows <= kMaxFusedNormRows && !prompt) {
             norm_w = w;
         } else {
             LAUNCH(m, K_NORM, st, launch_rmsnorm((const bf16*)in, w, c.rms_eps, rows, H, m->xn, st, false));
@@ -851,6 +982,13 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.sin_t = m->sin_t;
             a.layer = layer;
             a.rows = rm;
+            if (prompt) {
+                if (!amap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
+                LAUNCH(m, K_QKV, st,
+                       gemm_launch(m, a, &xm, &m->wmaps[layer].gq, &m->wmaps[layer].gk, &m->wmaps[layer].gv, st,
+                                   false));
+                break;
+            }
             if (!xmap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
             LAUNCH(m, K_QKV, st,
                    mv_launch(m, a, &m->wmaps[layer].q, &m->wmaps[layer].k, &m->wmaps[layer].v, &xm, st, false,
@@ -868,6 +1006,11 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             at.n_kv = c.n_kv;
             at.layer = layer;
             at.rows = rm;
+            if (prompt) {
+                const int e = prompt_attention(m, rm, layer, (const bf16*)in, (bf16*)out, st, false);
+                if (e) return e;
+                break;
+            }
             LAUNCH(m, K_ATTN, st, launch_attn_block(at, st, false));
             LAUNCH(m, K_MERGE, st, launch_attn_merge(at, st, false));
             break;
@@ -879,6 +1022,13 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.w0 = op == TFL_OP_O_RESIDUAL ? m->wo[layer] : m->wd[layer];
             a.n_out = H;
             a.h = (bf16*)out;
+            if (prompt) {
+                if (!amap(a.K)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
+                LAUNCH(m, op == TFL_OP_O_RESIDUAL ? K_O : K_DOWN, st,
+                       gemm_launch(m, a, &xm, op == TFL_OP_O_RESIDUAL ? &m->wmaps[layer].go : &m->wmaps[layer].gd,
+                                   nullptr, nullptr, st, false));
+                break;
+            }
             if (!xmap(a.K)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
             LAUNCH(m, op == TFL_OP_O_RESIDUAL ? K_O : K_DOWN, st,
                    mv_launch(m, a, op == TFL_OP_O_RESIDUAL ? &m->wmaps[layer].o : &m->wmaps[layer].d, nullptr,
@@ -892,6 +1042,12 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.n_out = c.ffn;
             a.y = (bf16*)out;
             a.ldy = c.ffn;
+            if (prompt) {
+                if (!amap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
+                LAUNCH(m, K_GATEUP, st,
+                       gemm_launch(m, a, &xm, &m->wmaps[layer].gg, &m->wmaps[layer].gu, nullptr, st, false));
+                break;
+            }
             if (!xmap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
             LAUNCH(m, K_GATEUP, st,
                    mv_launch(m, a, &m->wmaps[layer].g, &m->wmaps[layer].u, nullptr, &xm, st, false, norm_w));

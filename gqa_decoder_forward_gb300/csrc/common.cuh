@@ -111,6 +111,22 @@ cudaError_t init_matvec_tma();
 int matvec_norm_depth(int n_rows, int K);
 cudaError_t launch_matvec_tma(const MatvecTmaArgs& a, int grid, cudaStream_t st, bool pdl);
 
+// Prompt-chunk GEMM on tcgen05: activations [rows][K] through a 2-D map with
+// boxes of (64, 128 rows); weights 2-D with boxes of (64, 256) for STORE /
+// RESIDUAL, (64, 128) = one head for QKV_ROPE, (64, 64) for the gate and up
+// halves of SWIGLU.  e.n_rows is the chunk's row count; rows sit at positions
+// e.rows.pos0[0] + r of stream 0.
+struct GemmArgs {
+    MatvecArgs e;
+    CUtensorMap amap;
+    CUtensorMap bmap[3];
+    int m_tiles, n_tiles, kblocks;
+    int* status;
+};
+cudaError_t init_gemm_tc();
+int gemm_tile_n(int mode);
+cudaError_t launch_gemm_tc(const GemmArgs& a, int grid, cudaStream_t st, bool pdl);
+
 cudaError_t launch_embed_rmsnorm(const int32_t* ids, const bf16* embed, int vocab, const bf16* w, float eps,
                                  int n_rows, int H, bf16* h, bf16* xn, int* status, cudaStream_t st, bool pdl);
 cudaError_t launch_rmsnorm(const bf16* x, const bf16* w, float eps, int n_rows, int H, bf16* out,

@@ -281,14 +281,17 @@ def tfl_status(model: Model, stream=None) -> int:
     return int(lib().tfl_status(model.handle, _stream(stream)))
 
 
+TFL_OP_PROMPT = 0x100
 OPS = {"attn_norm": 0, "qkv_rope": 1, "attention": 2, "o_residual": 3, "ffn_norm": 4, "gate_up": 5,
        "down_residual": 6, "final_norm": 7, "lm_head": 8, "norm_qkv_rope": 9, "norm_gate_up": 10,
        "norm_lm_head": 11}
 
 
 def tfl_layer_op(model: Model, op: str, layer: int, inp: torch.Tensor, out: torch.Tensor, kv: "KV" = None,
-                 pos0: int = 0, stream=None):
-    return _check(lib().tfl_layer_op(model.handle, OPS[op], layer, kv.handle if kv is not None else None, pos0,
+                 pos0: int = 0, stream=None, prompt: bool = False):
+    """One op of the decode path (prompt=True: of the prompt-chunk path)."""
+    code = OPS[op] | (TFL_OP_PROMPT if prompt else 0)
+    return _check(lib().tfl_layer_op(model.handle, code, layer, kv.handle if kv is not None else None, pos0,
                                      inp.shape[0], _ptr(inp), _ptr(out), _stream(stream)))
 
 

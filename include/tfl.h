@@ -258,6 +258,11 @@ int tfl_head(tfl_model* model, const void* h, int rows, void* logits, void* stre
  *                        runs them: in is the residual stream h; the result is
  *                        bit-identical to the norm op followed by the projection op
  * Buffers are 16-byte aligned; in and out must not overlap.
+ * op | TFL_OP_PROMPT runs the op with the prompt-chunk kernels instead (rows
+ * 1..max_rows): the projections on the tensor-core GEMM, the norms always as a
+ * separate kernel, attention in windows of max_decode_rows rows.  Not for
+ * TFL_OP_LM_HEAD / TFL_OP_NORM_LM_HEAD (a prompt chunk's logits come from the
+ * decode head): TFL_E_ARG.
  */
 #define TFL_OP_ATTN_NORM 0
 #define TFL_OP_QKV_ROPE 1
@@ -271,6 +276,7 @@ int tfl_head(tfl_model* model, const void* h, int rows, void* logits, void* stre
 #define TFL_OP_NORM_QKV_ROPE 9
 #define TFL_OP_NORM_GATE_UP 10
 #define TFL_OP_NORM_LM_HEAD 11
+#define TFL_OP_PROMPT 0x100
 int tfl_layer_op(tfl_model* model, int op, int layer, tfl_kv* kv, int pos0, int rows, const void* in, void* out,
                  void* stream);
 

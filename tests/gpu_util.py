@@ -213,11 +213,11 @@ def bound_sum(out, acc):
     return ulp_of(out) + acc
 
 
-def check_ops(tfl, model, kv, layer, ch, pos0, report=None, head=None):
-    """Runs each decode op on the oracle's input of that op and gates its output:
-    single-rounding outputs with the plain ulp gate, fused ones with the
-    rounding-point bound.  head = (orc, hw, shape) also checks the final norm and
-    lm_head on the oracle's layer output."""
+def check_ops(tfl, model, kv, layer, ch, pos0, report=None, head=None, prompt=False):
+    """Runs each decode op (prompt=True: each prompt-chunk op) on the oracle's
+    input of that op and gates its output: single-rounding outputs with the
+    plain ulp gate, fused ones with the rounding-point bound.  head = (orc, hw,
+    shape) also checks the final norm and lm_head on the oracle's layer output."""
     R = ch["h_in"].shape[0]
     T = lambda a: to_torch_bits(np.ascontiguousarray(a).reshape(R, -1))  # noqa: E731
     res = {}
@@ -230,10 +230,10 @@ def check_ops(tfl, model, kv, layer, ch, pos0, report=None, head=None):
             res[name] = assert_bound_gate(g, ref, bound, f"layer {layer} {name}")
 
     out = torch.empty_like(T(ch["xn1"]))
-    tfl.tfl_layer_op(model, "attn_norm", layer, T(ch["h_in"]), out)
+    tfl.tfl_layer_op(model, "attn_norm", layer, T(ch["h_in"]), out, prompt=prompt)
     gate("attn_norm", out, ch["xn1"], bound_norm(ch["y1"], model_norm(model, "attn_norm", layer), ch["xn1"]))
     q = torch.empty_like(T(ch["q"]))
-    tfl.tfl_layer_op(model, "qkv_rope", layer, T(ch["xn1"]), q, kv, pos0)
+    tfl.tfl_layer_op(model, "qkv_rope", layer, T(ch["xn1"]), q, kv, pos0, prompt=prompt)
     H, QD, F = ch["K"]
     gate("qkv_rope.q", q, ch["q"],
          bound_rope(ch["qp"], ch["cos"], ch["sin"], ch["q"], acc_allowance(ch["qp_abs"], H)))
@@ -244,20 +244,20 @@ def check_ops(tfl, model, kv, layer, ch, pos0, report=None, head=None):
     # the attention reads the oracle's keys and values for the call's own rows
     kv.write(layer, pos0, to_torch_bits(ch["k"]), to_torch_bits(ch["v"]))
     o = torch.empty_like(T(ch["o"]))
-    tfl.tfl_layer_op(model, "attention", layer, T(ch["q"]), o, kv, pos0)
+    tfl.tfl_layer_op(model, "attention", layer, T(ch["q"]), o, kv, pos0, prompt=prompt)
     gate("attention", o, ch["o"], bound_sum(ch["o"], acc_allowance(ch["o_abs"], ch["n_keys"])))
     h = T(ch["h_in"]).clone()
-    tfl.tfl_layer_op(model, "o_residual", layer, T(ch["o"]), h)
+    tfl.tfl_layer_op(model, "o_residual", layer, T(ch["o"]), h, prompt=prompt)
     gate("o_residual", h, ch["h1"], bound_residual(ch["yo"], ch["h1"], acc_allowance(ch["yo_abs"], QD)))
     xn2 = torch.empty_like(h)
-    tfl.tfl_layer_op(model, "ffn_norm", layer, T(ch["h1"]), xn2)
+    tfl.tfl_layer_op(model, "ffn_norm", layer, T(ch["h1"]), xn2, prompt=prompt)
     gate("ffn_norm", xn2, ch["xn2"], bound_norm(ch["y2"], model_norm(model, "ffn_norm", layer), ch["xn2"]))
     a = torch.empty_like(T(ch["a"]))
-    tfl.tfl_layer_op(model, "gate_up", layer, T(ch["xn2"]), a)
+    tfl.tfl_layer_op(model, "gate_up", layer, T(ch["xn2"]), a, prompt=prompt)
     gate("gate_up", a, ch["a"], bound_swiglu(ch["g"], ch["u"], ch["sg"], ch["a"], acc_allowance(ch["g_abs"], H),
                                              acc_allowance(ch["u_abs"], H)))
     h = T(ch["h1"]).clone()
-    tfl.tfl_layer_op(model, "down_residual", layer, T(ch["a"]), h)
+    tfl.tfl_layer_op(model, "down_residual", layer, T(ch["a"]), h, prompt=prompt)
     gate("down_residual", h, ch["h2"], bound_residual(ch["yd"], ch["h2"], acc_allowance(ch["yd_abs"], F)))
     if head is not None:
         orc, hw, shape = head

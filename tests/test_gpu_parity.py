@@ -285,6 +285,151 @@ def test_33b_layer_steps_equal_windows(layer33, R):
     assert torch.equal(va.view(torch.int16), vb.view(torch.int16))
 
 
+# ---- the prompt-chunk path (tensor-core GEMM projections) -------------------------------
+
+@pytest.mark.parametrize("R", [1, 200])
+def test_tiny_prompt_ops_every_layer(orc, tiny, R):
+    """Each prompt-chunk op (projections on the tensor-core GEMM over 128-row
+    tiles with a ragged tail) fed the oracle's bf16 inputs, gated like the
+    decode ops."""
+    w, hw = tiny
+    m = _tiny_model(w, max_context=512)
+    kv = m.kv(512)
+    P = 40
+    ids = synth.uniform_ids(3, P + R, TINY.vocab, "cuda")
+    om = gu.oracle_model(orc, TINY, hw, 512)
+    _, trace = om.forward(ids.cpu().numpy(), np.arange(P + R, dtype=np.int32), want_logits=False,
+                          want_trace=True)
+    pos = np.arange(P, P + R, dtype=np.int32)
+    for l in range(TINY.layers):
+        kv.write(l, 0, gu.to_torch_bits(om.K[l, :P]), gu.to_torch_bits(om.V[l, :P]))
+        ch = gu.oracle_chain(orc, TINY, hw, l, trace[l][P:], pos, om.K[l, :P], om.V[l, :P])
+        gu.check_ops(tfl, m, kv, l, ch, P, prompt=True)
+
+
+def test_33b_prompt_ops(orc, layer33):
+    """The prompt ops of a 33B-shaped layer over 130 rows (two 128-row tiles, the
+    second ragged) after a seeded 4,096-position cache."""
+    w, hw, K, V = layer33
+    R = 130
+    m = tfl.Model(L1, w, max_decode_rows=16, max_rows=R, max_context=4352)
+    kv = _seeded(m, K, V, 4352)
+    h_in = synth.bits(synth.hidden_rows(L1, 15, R, "cuda"))
+    pos = np.arange(4096, 4096 + R, dtype=np.int32)
+    ch = gu.oracle_chain(orc, L1, hw, 0, h_in, pos, synth.bits(K), synth.bits(V))
+    gu.check_ops(tfl, m, kv, 0, ch, 4096, prompt=True)
+
+
+SAMPLED = np.array([0, 1, 127, 128, 1023, 1500, 2047])
+
+
+def test_33b_full_chunk_projections_sampled(orc, layer33):
+    """A full 2,048-row chunk through each prompt GEMM (the launch configuration
+    the benchmark times); sampled rows against the oracle, gated as the ops."""
+    w, hw, K, V = layer33
+    N, H, QD, F, D = 2048, L1.hidden, L1.n_q * 128, L1.ffn, 128
+    m = tfl.Model(L1, w, max_decode_rows=64, max_rows=N, max_context=4096 + N)
+    kv = _seeded(m, K, V, 4096 + N)
+    S = SAMPLED
+    pos = 4096 + S.astype(np.int32)
+    c, s = orc.rope_table(L1.rope_theta, D, 4096 + N)
+    A = gu.abs_bits
+
+    def gate(name, got, ref, bound):
+        gu.assert_bound_gate(synth.bits(got)[S].reshape(ref.shape), ref, bound, name)
+
+    # QKV + RoPE, keys/values into the cache
+    xn = synth.normal_bf16(21, 0, (N, H), 1.0, "cuda")
+    q = torch.empty((N, QD), dtype=torch.bfloat16, device="cuda")
+    tfl.tfl_layer_op(m, "qkv_rope", 0, xn, q, kv, 4096, prompt=True)
+    x = synth.bits(xn)[S]
+    for name, wk, nh in (("q", "wq", L1.n_q), ("k", "wk", L1.n_kv)):
+        pre = orc.linear(hw[wk][0], x).reshape(len(S), nh, D)
+        pre_abs = orc.linear(A(hw[wk][0]), A(x)).reshape(len(S), nh, D)
+        ref = orc.rope_apply(pre, pos, c, s)
+        bound = gu.bound_rope(pre, c[pos], s[pos], ref, gu.acc_allowance(pre_abs, H))
+        if name == "q":
+            gate("q", q, ref, bound)
+        else:
+            k_got = torch.stack([kv.read(0, int(p), 1)[0][0] for p in pos])
+            gu.assert_bound_gate(synth.bits(k_got).reshape(ref.shape), ref, bound, "k")
+    v_ref = orc.linear(hw["wv"][0], x).reshape(len(S), L1.n_kv, D)
+    v_abs = orc.linear(A(hw["wv"][0]), A(x)).reshape(len(S), L1.n_kv, D)
+    v_got = torch.stack([kv.read(0, int(p), 1)[1][0] for p in pos])
+    gu.assert_bound_gate(synth.bits(v_got).reshape(v_ref.shape), v_ref,
+                         gu.bound_sum(v_ref, gu.acc_allowance(v_abs, H)), "v")
+
+    # o projection + residual, in place
+    o = synth.normal_bf16(22, 0, (N, QD), 0.5, "cuda")
+    h = synth.hidden_rows(L1, 23, N, "cuda", std=0.5)
+    h0 = synth.bits(h)[S]
+    tfl.tfl_layer_op(m, "o_residual", 0, o, h, prompt=True)
+    yo = orc.linear(hw["wo"][0], synth.bits(o)[S])
+    yo_abs = orc.linear(A(hw["wo"][0]), A(synth.bits(o)[S]))
+    ref = orc.residual_add(h0, yo)
+    gate("o_residual", h, ref, gu.bound_residual(yo, ref, gu.acc_allowance(yo_abs, QD)))
+
+    # gate/up + SwiGLU
+    act = torch.empty((N, F), dtype=torch.bfloat16, device="cuda")
+    tfl.tfl_layer_op(m, "gate_up", 0, xn, act, prompt=True)
+    g = orc.linear(hw["wg"][0], x)
+    u = orc.linear(hw["wu"][0], x)
+    ref = orc.swiglu(g, u)
+    sg = orc.swiglu(g, np.full_like(g, 0x3F80))
+    gate("gate_up", act, ref, gu.bound_swiglu(g, u, sg, ref, gu.acc_allowance(orc.linear(A(hw["wg"][0]), A(x)), H),
+                                             gu.acc_allowance(orc.linear(A(hw["wu"][0]), A(x)), H)))
+
+    # down projection + residual
+    a_in = synth.normal_bf16(24, 0, (N, F), 0.1, "cuda")
+    h = synth.hidden_rows(L1, 25, N, "cuda", std=0.5)
+    h0 = synth.bits(h)[S]
+    tfl.tfl_layer_op(m, "down_residual", 0, a_in, h, prompt=True)
+    yd = orc.linear(hw["wd"][0], synth.bits(a_in)[S])
+    yd_abs = orc.linear(A(hw["wd"][0]), A(synth.bits(a_in)[S]))
+    ref = orc.residual_add(h0, yd)
+    gate("down_residual", h, ref, gu.bound_residual(yd, ref, gu.acc_allowance(yd_abs, F)))
+    torch.cuda.synchronize()
+
+
+def test_33b_prompt_chunking_is_bit_exact(layer33):
+    """A 2,048-row prompt chunk equals the same rows split into chunks of 700, 1
+    and 1,347 rows (row results independent of chunk boundaries and tiles)."""
+    w, _, K, V = layer33
+    N = 2048
+    m = tfl.Model(L1, w, max_decode_rows=64, max_rows=N, max_context=4096 + N)
+    h_in = synth.hidden_rows(L1, 16, N, "cuda")
+    a = _seeded(m, K, V, 4096 + N)
+    whole = torch.empty_like(h_in)
+    tfl.tfl_prefill_hidden(m, a, h_in, whole)
+    b = _seeded(m, K, V, 4096 + N)
+    parts = torch.empty_like(h_in)
+    r0 = 0
+    for n in (700, 1, 1347):
+        tfl.tfl_prefill_hidden(m, b, h_in[r0:r0 + n].contiguous(), parts[r0:r0 + n])
+        r0 += n
+    assert a.length == b.length == 4096 + N
+    assert torch.equal(whole.view(torch.int16), parts.view(torch.int16))
+    ka, va = a.read(0, 4096, N)
+    kb, vb = b.read(0, 4096, N)
+    assert torch.equal(ka.view(torch.int16), kb.view(torch.int16))
+    assert torch.equal(va.view(torch.int16), vb.view(torch.int16))
+    assert bool(torch.isfinite(whole.float()).all())
+
+
+def test_prompt_op_arguments_are_checked(tiny):
+    w, _ = tiny
+    m = _tiny_model(w, max_rows=256)
+    x = torch.zeros((257, TINY.hidden), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    with pytest.raises(tfl.TflError) as e:
+        tfl.tfl_layer_op(m, "ffn_norm", 0, x, y, prompt=True)
+    assert e.value.code == tfl.TFL_E_ARG
+    lg = torch.empty((4, TINY.vocab), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(tfl.TflError) as e:
+        tfl.tfl_layer_op(m, "lm_head", 0, x[:4], lg, prompt=True)
+    assert e.value.code == tfl.TFL_E_ARG
+
+
 # ---- argmax, status, capacity ---------------------------------------------------------
 
 def test_argmax_ties_and_nonfinite(orc, tiny):
