@@ -202,10 +202,15 @@ constexpr int kMaxFusedNormRows = 8;
 // ---- model / kv objects --------------------------------------------------------
 
 // Kernel families timed by tfl_profile (names in tfl_profile_kind).
-enum Kind { K_EMBED, K_NORM, K_QKV, K_ATTN, K_MERGE, K_O, K_GATEUP, K_DOWN, K_LMHEAD, K_ARGMAX, K_COUNT };
+enum Kind {
+    K_EMBED, K_NORM, K_QKV, K_ATTN, K_MERGE, K_O, K_GATEUP, K_DOWN, K_LMHEAD, K_ARGMAX,
+    K_GQKV, K_GO, K_GGATEUP, K_GDOWN, K_PATTN, K_COUNT
+};
 const char* const kKindName[K_COUNT] = {"embed_rmsnorm", "rmsnorm", "matvec_qkv_rope", "attn_decode_block",
                                         "attn_decode_merge", "matvec_o_residual", "matvec_gate_up_swiglu",
-                                        "matvec_down_residual", "matvec_lm_head", "argmax"};
+                                        "matvec_down_residual", "matvec_lm_head", "argmax",
+                                        "gemm_qkv_rope", "gemm_o_residual", "gemm_gate_up_swiglu",
+                                        "gemm_down_residual", "attn_prefill"};
 
 struct Mark {
     int kind;
@@ -502,33 +507,21 @@ cudaError_t gemm_launch(tfl_model* m, const MatvecArgs& e, const CUtensorMap* am
     return launch_gemm_tc(g, m->grid, st, pdl);
 }
 
-// Attention of the rows of a prompt chunk (one stream, queries q, output out,
-// both [rows][n_q*128]) through the decode attention kernels, in windows of
-// max_decode_rows rows; each row's result is independent of the windowing.
+// Causal attention of the rows of a prompt chunk (one stream, queries q,
+// output out, both [rows][n_q*128]) in one launch of the prefill kernel.
 int prompt_attention(tfl_model* m, const RowMap& rm, int layer, const bf16* q, bf16* out, cudaStream_t st,
                      bool pdl) {
     const tfl_config& c = m->cfg;
-    const int qd = c.n_q * kHeadDim;
-    for (int w0 = 0; w0 < rm.n_rows; w0 += c.max_decode_rows) {
-        const int k = std::min(c.max_decode_rows, rm.n_rows - w0);
-        AttnDecodeArgs at = {};
-        at.q = q + (size_t)w0 * qd;
-        at.out = out + (size_t)w0 * qd;
-        at.pm = m->pm;
-        at.pl = m->pl;
-        at.po = m->po;
-        at.max_blocks = m->L.max_blocks;
-        at.n_q = c.n_q;
-        at.n_kv = c.n_kv;
-        at.layer = layer;
-        at.rows.n_streams = 1;
-        at.rows.n_rows = k;
-        at.rows.row_start[1] = k;
-        at.rows.pos0[0] = rm.pos0[0] + w0;
-        at.rows.kv[0] = rm.kv[0];
-        LAUNCH(m, K_ATTN, st, launch_attn_block(at, st, pdl));
-        LAUNCH(m, K_MERGE, st, launch_attn_merge(at, st, pdl));
-    }
+    AttnPrefillArgs p = {};
+    p.q = q;
+    p.out = out;
+    p.kv = rm.kv[0];
+    p.n_q = c.n_q;
+    p.n_kv = c.n_kv;
+    p.layer = layer;
+    p.pos0 = rm.pos0[0];
+    p.n_rows = rm.n_rows;
+    LAUNCH(m, K_PATTN, st, launch_attn_prefill(p, st, pdl));
     return TFL_OK;
 }
 
@@ -563,7 +556,7 @@ int run_prompt_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const 
         a.sin_t = m->sin_t;
         a.layer = l;
         a.rows = rm;
-        LAUNCH(m, K_QKV, st, gemm_launch(m, a, &m->amap_xn, &wm.gq, &wm.gk, &wm.gv, st, pdl));
+        LAUNCH(m, K_GQKV, st, gemm_launch(m, a, &m->amap_xn, &wm.gq, &wm.gk, &wm.gv, st, pdl));
         int e = prompt_attention(m, rm, l, m->q, m->ao, st, pdl);
         if (e) return e;
         MatvecArgs o = {};
@@ -572,7 +565,7 @@ int run_prompt_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const 
         o.n_rows = n;
         o.n_out = H;
         o.h = m->h;
-        LAUNCH(m, K_O, st, gemm_launch(m, o, &m->amap_ao, &wm.go, nullptr, nullptr, st, pdl));
+        LAUNCH(m, K_GO, st, gemm_launch(m, o, &m->amap_ao, &wm.go, nullptr, nullptr, st, pdl));
         LAUNCH(m, K_NORM, st, launch_rmsnorm(m->h, m->ffn_norm[l], c.rms_eps, n, H, m->xn, st, pdl));
         MatvecArgs gu = {};
         gu.mode = MV_SWIGLU;
@@ -581,14 +574,14 @@ int run_prompt_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const 
         gu.n_out = c.ffn;
         gu.y = m->act;
         gu.ldy = c.ffn;
-        LAUNCH(m, K_GATEUP, st, gemm_launch(m, gu, &m->amap_xn, &wm.gg, &wm.gu, nullptr, st, pdl));
+        LAUNCH(m, K_GGATEUP, st, gemm_launch(m, gu, &m->amap_xn, &wm.gg, &wm.gu, nullptr, st, pdl));
         MatvecArgs d = {};
         d.mode = MV_RESIDUAL;
         d.K = c.ffn;
         d.n_rows = n;
         d.n_out = H;
         d.h = m->h;
-        LAUNCH(m, K_DOWN, st, gemm_launch(m, d, &m->amap_act, &wm.gd, nullptr, nullptr, st, pdl));
+        LAUNCH(m, K_GDOWN, st, gemm_launch(m, d, &m->amap_act, &wm.gd, nullptr, nullptr, st, pdl));
     }
     return TFL_OK;
 }
@@ -772,6 +765,7 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
         cudaError_t ce0 = cudaSuccess;
         if (okm) ce0 = init_matvec_tma();
         if (okm && ce0 == cudaSuccess) ce0 = init_gemm_tc();
+        if (okm && ce0 == cudaSuccess) ce0 = init_attn_prefill();
         if (!okm || ce0 != cudaSuccess) {
             delete m;
             return fail(TFL_E_CUDA, "building TMA descriptors failed%s%s", ce0 ? ": " : "",
@@ -984,7 +978,7 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.rows = rm;
             if (prompt) {
                 if (!amap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
-                LAUNCH(m, K_QKV, st,
+                LAUNCH(m, K_GQKV, st,
                        gemm_launch(m, a, &xm, &m->wmaps[layer].gq, &m->wmaps[layer].gk, &m->wmaps[layer].gv, st,
                                    false));
                 break;
@@ -1024,7 +1018,7 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.h = (bf16*)out;
             if (prompt) {
                 if (!amap(a.K)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
-                LAUNCH(m, op == TFL_OP_O_RESIDUAL ? K_O : K_DOWN, st,
+                LAUNCH(m, op == TFL_OP_O_RESIDUAL ? K_GO : K_GDOWN, st,
                        gemm_launch(m, a, &xm, op == TFL_OP_O_RESIDUAL ? &m->wmaps[layer].go : &m->wmaps[layer].gd,
                                    nullptr, nullptr, st, false));
                 break;
@@ -1044,7 +1038,7 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             a.ldy = c.ffn;
             if (prompt) {
                 if (!amap(H)) return fail(TFL_E_ARG, "cannot describe the input rows to TMA");
-                LAUNCH(m, K_GATEUP, st,
+                LAUNCH(m, K_GGATEUP, st,
                        gemm_launch(m, a, &xm, &m->wmaps[layer].gg, &m->wmaps[layer].gu, nullptr, st, false));
                 break;
             }

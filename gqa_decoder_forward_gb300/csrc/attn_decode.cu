@@ -26,6 +26,7 @@
 // row of P.  A row gives the same bits alone or beside other rows (one-row
 // steps == windows, solo == batched).
 #include "common.cuh"
+#include "warp_mma.cuh"
 
 namespace tfl {
 namespace {
@@ -46,36 +47,12 @@ struct Smem {
     float wsum[kWarps][kMaxPairs];   // per-warp row sums
 };
 
-__device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, bool valid) {
-    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-    const int src = valid ? 16 : 0;  // 0 source bytes: the 16 destination bytes are zero-filled
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sa), "l"(gmem), "r"(src));
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
-    const unsigned a = (unsigned)__cvta_generic_to_shared(p);
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(a));
-}
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(bf16 lo, bf16 hi) {
-    return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
-}
+using wm::cp_async16_zfill;
+using wm::cp_async_wait_all;
+using wm::ldsm_x4;
+using wm::ldsm_x4_t;
+using wm::mma16816;
+using wm::pack_bf16;
 
 // Locates row group z: stream s, first row (global index) r0, row count nr.
 __device__ __forceinline__ bool find_group(const RowMap& m, int z, int& s, int& r0, int& nr) {

@@ -146,6 +146,18 @@ cudaError_t init_attn_decode();
 cudaError_t launch_attn_block(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
 cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl);
 
+// Causal attention of the rows of one prompt chunk (one stream): row r at
+// position pos0 + r attends keys 0 .. pos0 + r of kv (layer).
+struct AttnPrefillArgs {
+    const bf16* q;        // [n_rows][n_q*D] rotated
+    bf16* out;            // [n_rows][n_q*D]
+    KvView kv;
+    int n_q, n_kv, layer;
+    int pos0, n_rows;
+};
+cudaError_t init_attn_prefill();
+cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t st, bool pdl);
+
 cudaError_t launch_argmax(const bf16* logits, int n_rows, int V, int32_t* ids, int* status, cudaStream_t st,
                           bool pdl);
 

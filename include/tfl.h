@@ -260,7 +260,7 @@ int tfl_head(tfl_model* model, const void* h, int rows, void* logits, void* stre
  * Buffers are 16-byte aligned; in and out must not overlap.
  * op | TFL_OP_PROMPT runs the op with the prompt-chunk kernels instead (rows
  * 1..max_rows): the projections on the tensor-core GEMM, the norms always as a
- * separate kernel, attention in windows of max_decode_rows rows.  Not for
+ * separate kernel, attention by the one-pass causal prompt kernel.  Not for
  * TFL_OP_LM_HEAD / TFL_OP_NORM_LM_HEAD (a prompt chunk's logits come from the
  * decode head): TFL_E_ARG.
  */
