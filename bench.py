@@ -49,6 +49,8 @@ def parse():
                    help="time one decode op (qkv_rope, attention, o_residual, gate_up, down_residual, attn_norm) "
                         "on a one-layer 33B-shaped model instead of the full step")
     p.add_argument("--rows", type=int, default=1, help="rows per step for --op")
+    p.add_argument("--prompt", action="store_true",
+                   help="--op runs the prompt-chunk kernel of the op (rows up to 2,048)")
     return p.parse_args()
 
 
@@ -224,6 +226,30 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def ncu_traffic(kernel):
+    """DRAM bytes per launch of a kernel family from the committed ncu summary
+    (profiles/ncu_traffic.md), or None when its sources changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+    if not os.path.exists(path):
+        return None
+    csrc = os.path.join(ROOT, "gqa_decoder_forward_gb300", "csrc")
+    with open(path) as fh:
+        for line in fh:
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) != 5 or cells[0] != kernel:
+                continue
+            m = hashlib.sha256()
+            for f in cells[3].split():
+                fp = os.path.join(csrc, f)
+                if not os.path.exists(fp):
+                    return None
+                with open(fp, "rb") as src:
+                    m.update(src.read())
+            return int(cells[2]) if m.hexdigest()[:16] == cells[4] else None
+    return None
+
+
 def bf16_peak():
     """Dense bf16 tensor peak (TFLOP/s): the measured sustained cuBLAS figure (a
     prefill runs for about a second), else the fallback."""
@@ -252,7 +278,7 @@ def prefill_roofline(shape, ctx, prof):
     peak, kind = bf16_peak()
     return {"bound": "tensor", "kernel": best, "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
             "frac": round(achieved / peak, 4), "peak_kind": kind, "launches": n,
-            "ms_per_launch": round(ms / n, 4), "traffic": None}
+            "ms_per_launch": round(ms / n, 4), "traffic": ncu_traffic(best)}
 
 
 def run_tfl(args, world, rank, local):
@@ -371,7 +397,7 @@ def run_tfl(args, world, rank, local):
     if dom_bytes is not None:
         ach = dom_bytes / (dom_ms / dom_n / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": dom_name, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                "frac": round(ach / peak, 4), "traffic": ncu_traffic(dom_name), "peak_kind": peak_kind,
                 "bytes_per_launch": dom_bytes, "us_per_launch": round(dom_ms / dom_n * 1e3, 2)}
 
     cpu = None
@@ -424,30 +450,36 @@ def run_op(args):
     w["final_norm"] = torch.ones(one.hidden, dtype=torch.bfloat16, device=dev)
     w["lm_head"] = torch.zeros(64, dtype=torch.bfloat16, device=dev)
     R, ctx = args.rows, args.context
-    m = tfl.Model(one, w, max_rows=64, max_decode_rows=64, max_context=ctx + R)
+    m = tfl.Model(one, w, max_rows=max(64, R), max_decode_rows=64, max_context=ctx + R)
     kv = m.kv(ctx + R)
     K, V = synth.kv_contents(one, 22, 0, ctx + R, dev)
     kv.write(0, 0, K, V)
     H, QD, F = one.hidden, one.n_q * 128, one.ffn
     x = {"attn_norm": (H, H), "qkv_rope": (H, QD), "attention": (QD, QD), "o_residual": (QD, H),
-         "gate_up": (H, F), "down_residual": (F, H)}[args.op]
+         "gate_up": (H, F), "down_residual": (F, H), "norm_qkv_rope": (H, QD), "norm_gate_up": (H, F)}[args.op]
     inp = synth.normal_bf16(5, 5, (R, x[0]), 1.0, dev)
     out = synth.normal_bf16(6, 6, (R, x[1]), 1.0, dev)
     for _ in range(args.warmup):
-        tfl.tfl_layer_op(m, args.op, 0, inp, out, kv, ctx)
+        tfl.tfl_layer_op(m, args.op, 0, inp, out, kv, ctx, prompt=args.prompt)
     torch.cuda.synchronize()
     st = torch.cuda.current_stream()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(st)
     for _ in range(args.steps):
-        tfl.tfl_layer_op(m, args.op, 0, inp, out, kv, ctx)
+        tfl.tfl_layer_op(m, args.op, 0, inp, out, kv, ctx, prompt=args.prompt)
     t1.record(st)
     torch.cuda.synchronize()
     us = t0.elapsed_time(t1) / args.steps * 1e3
     wbytes = {"attn_norm": 2 * H, "qkv_rope": (QD + 2 * 1024) * H * 2, "attention": 2 * 1024 * 2 * (ctx + R),
-              "o_residual": H * QD * 2, "gate_up": 2 * F * H * 2, "down_residual": H * F * 2}[args.op]
-    print(json.dumps({"op": args.op, "rows": R, "context": ctx, "us_per_launch": round(us, 2),
-                      "bytes": wbytes, "gbs": round(wbytes / us / 1e3, 1)}), flush=True)
+              "o_residual": H * QD * 2, "gate_up": 2 * F * H * 2, "down_residual": H * F * 2,
+              "norm_qkv_rope": (QD + 2 * 1024) * H * 2, "norm_gate_up": 2 * F * H * 2}[args.op]
+    flops = 2.0 * R * {"attn_norm": 0, "qkv_rope": (QD + 2 * 1024) * H, "o_residual": H * QD,
+                       "norm_qkv_rope": (QD + 2 * 1024) * H, "norm_gate_up": 2 * F * H,
+                       "gate_up": 2 * F * H, "down_residual": H * F,
+                       "attention": one.n_q * 128 * 2 * (ctx + (R + 1) / 2)}[args.op]
+    print(json.dumps({"op": args.op, "prompt": args.prompt, "rows": R, "context": ctx, "us_per_launch": round(us, 2),
+                      "bytes": wbytes, "gbs": round(wbytes / us / 1e3, 1),
+                      "tflops": round(flops / us / 1e6, 1)}), flush=True)
 
 
 def main():

@@ -35,20 +35,29 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRB = 4;               // rows per CTA
 constexpr int kKB = kPage;           // keys per block
-constexpr int kPad = kHeadDim + 8;   // padded row (bf16): 272 bytes, conflict-free ldmatrix
 constexpr int kMaxPairs = 32;        // kRB rows x up to 8 heads, two m16 tiles
+constexpr int kMergeSlices = 8;      // block slices of one merge CTA
 
+// Rows of 128 bf16 (256 bytes, 16 chunks of 16 bytes) with chunk c of row r
+// stored at chunk c ^ (r & 7): the eight rows an ldmatrix reads hit distinct
+// banks without padding.
+__device__ __forceinline__ int swz(int row, int col) {
+    return row * kHeadDim + (((col >> 3) ^ (row & 7)) << 3) + (col & 7);
+}
+
+// 75,776 bytes: three CTAs per SM.  The softmax weights (hi and lo parts,
+// 2 x 32 x 128 bf16) reuse the key tile once the scores are computed.
 struct Smem {
-    bf16 q[kMaxPairs][kPad];         // 8.5 KB
-    bf16 k[kKB][kPad];               // 34 KB
-    bf16 v[kKB][kPad];               // 34 KB
-    bf16 p[2][kMaxPairs][kPad];      // 17 KB: softmax weights, hi and lo parts
+    bf16 q[kMaxPairs * kHeadDim];    // 8 KB
+    bf16 k[kKB * kHeadDim];          // 32 KB (then the weights)
+    bf16 v[kKB * kHeadDim];          // 32 KB
     float wmax[kWarps][kMaxPairs];   // per-warp row maxima
     float wsum[kWarps][kMaxPairs];   // per-warp row sums
 };
 
 using wm::cp_async16_zfill;
-using wm::cp_async_wait_all;
+using wm::cp_async_commit;
+using wm::cp_async_wait;
 using wm::ldsm_x4;
 using wm::ldsm_x4_t;
 using wm::mma16816;
@@ -72,10 +81,9 @@ __device__ __forceinline__ bool find_group(const RowMap& m, int z, int& s, int& 
 
 // G = query heads per KV head.  Pair p = i*G + j is (row i of the group, head g*G + j).
 template <int G>
-__global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_constant__ AttnDecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) attn_block_kernel(const __grid_constant__ AttnDecodeArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
-    pdl_wait();
 
     int s, r0, nr;
     if (!find_group(a.rows, blockIdx.z, s, r0, nr)) return;
@@ -91,17 +99,34 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
     const int MT = (P + 15) / 16;  // m16 tiles of pairs
 
     // stage keys and values of head g (rows of 256 B inside one page); keys past
-    // nv are zero-filled so that their weight-0 products stay exact zeros
+    // nv are zero-filled so that their weight-0 products stay exact zeros.  Keys
+    // first, values second, as two copy groups.
     const KvView& kv = a.rows.kv[s];
     const bf16* kbase = kv_row(kv, a.layer, 0, k0, a.n_kv) + (size_t)g * kHeadDim;
     const bf16* vbase = kv_row(kv, a.layer, 1, k0, a.n_kv) + (size_t)g * kHeadDim;
     const size_t pstride = (size_t)a.n_kv * kHeadDim;
-    for (int i = tid; i < kKB * 16; i += kThreads) {
-        const int t = i >> 4, c = i & 15;
-        const bool valid = t < nv;
-        const size_t off = valid ? t * pstride + c * 8 : 0;
-        cp_async16_zfill(&sm.k[t][c * 8], kbase + off, valid);
-        cp_async16_zfill(&sm.v[t][c * 8], vbase + off, valid);
+    auto stage = [&](bf16* dst, const bf16* src) {
+        for (int i = tid; i < kKB * 16; i += kThreads) {
+            const int t = i >> 4, c = i & 15;
+            const bool valid = t < nv;
+            cp_async16_zfill(dst + swz(t, c * 8), src + (valid ? t * pstride + c * 8 : 0), valid);
+        }
+        cp_async_commit();
+    };
+    // A block whose keys all precede the stream's first row of this call holds
+    // cache rows written by earlier calls (every kernel of the library signals
+    // its dependents only after its own dependency wait, so those writers have
+    // completed): it streams in while the previous kernel is still finishing.
+    const bool early = k0 + nv <= a.rows.pos0[s];
+    if (early) {
+        stage(sm.k, kbase);
+        stage(sm.v, vbase);
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (!early) {
+        stage(sm.k, kbase);
+        stage(sm.v, vbase);
     }
     // queries (bf16, unscaled); pairs past P are zero
     for (int i = tid; i < MT * 16 * 16; i += kThreads) {
@@ -112,9 +137,9 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
             val = *reinterpret_cast<const uint4*>(a.q + (size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim +
                                                    c * 8);
         }
-        *reinterpret_cast<uint4*>(&sm.q[p][c * 8]) = val;
+        *reinterpret_cast<uint4*>(&sm.q[swz(p, c * 8)]) = val;
     }
-    cp_async_wait_all();
+    cp_async_wait<1>();  // the keys have landed; the values may still be in flight
     __syncthreads();
 
     // ---- S = Q K^T: warp w owns keys 16w .. 16w+15 (two n8 tiles) ----
@@ -130,12 +155,12 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
 #pragma unroll
         for (int ks = 0; ks < kHeadDim / 16; ++ks) {
             uint32_t bk[4];
-            ldsm_x4(bk, &sm.k[warp * 16 + krow][ks * 16 + kcol]);
+            ldsm_x4(bk, &sm.k[swz(warp * 16 + krow, ks * 16 + kcol)]);
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
                 if (mt < MT) {
                     uint32_t aq[4];
-                    ldsm_x4(aq, &sm.q[mt * 16 + mrow][ks * 16 + mcol]);
+                    ldsm_x4(aq, &sm.q[swz(mt * 16 + mrow, ks * 16 + mcol)]);
                     mma16816(sc[mt][0], aq, bk[0], bk[1]);
                     mma16816(sc[mt][1], aq, bk[2], bk[3]);
                 }
@@ -174,6 +199,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
     }
     __syncthreads();
     // block row maxima, weights, per-warp row sums, weights to shared memory
+    // (over the key tile, which no warp reads any more)
+    bf16* pw = sm.k;
     float bmax[2][2];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
@@ -197,14 +224,15 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
                 const bf16 h0 = rn(e0), h1 = rn(e1);
                 const bf16 l0 = rn(e0 - bf(h0)), l1 = rn(e1 - bf(h1));
                 const int t = warp * 16 + nt * 8 + 2 * tig;
-                *reinterpret_cast<uint32_t*>(&sm.p[0][p][t]) = pack_bf16(h0, h1);
-                *reinterpret_cast<uint32_t*>(&sm.p[1][p][t]) = pack_bf16(l0, l1);
+                *reinterpret_cast<uint32_t*>(&pw[swz(p, t)]) = pack_bf16(h0, h1);
+                *reinterpret_cast<uint32_t*>(&pw[kMaxPairs * kHeadDim + swz(p, t)]) = pack_bf16(l0, l1);
             }
             l += __shfl_xor_sync(0xffffffffu, l, 1);
             l += __shfl_xor_sync(0xffffffffu, l, 2);
             if (tig == 0) sm.wsum[warp][p] = l;
         }
     }
+    cp_async_wait<0>();  // the values
     __syncthreads();
 
     // ---- O = P V: warp w owns dims 16w .. 16w+15 (two n8 tiles) ----
@@ -219,14 +247,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
 #pragma unroll 2
         for (int ks = 0; ks < kKB / 16; ++ks) {
             uint32_t bv[4];
-            ldsm_x4_t(bv, &sm.v[ks * 16 + vrow][warp * 16 + vcol]);
+            ldsm_x4_t(bv, &sm.v[swz(ks * 16 + vrow, warp * 16 + vcol)]);
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt) {
                 if (mt < MT) {
 #pragma unroll
                     for (int part = 0; part < 2; ++part) {
                         uint32_t ap[4];
-                        ldsm_x4(ap, &sm.p[part][mt * 16 + mrow][ks * 16 + mcol]);
+                        ldsm_x4(ap, &pw[part * kMaxPairs * kHeadDim + swz(mt * 16 + mrow, ks * 16 + mcol)]);
                         mma16816(oc[mt][0], ap, bv[0], bv[1]);
                         mma16816(oc[mt][1], ap, bv[2], bv[3]);
                     }
@@ -234,7 +262,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
             }
         }
     }
-    pdl_trigger();
 
     // ---- partials: o (unnormalised), m, l per (row, head) ----
 #pragma unroll
@@ -260,55 +287,75 @@ __global__ void __launch_bounds__(kThreads, 2) attn_block_kernel(const __grid_co
     }
 }
 
-// One CTA per (head, row).  Each thread owns one output dim and folds the blocks
-// in order; loads of later blocks are issued ahead (unrolled) to hide latency.
-__global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const __grid_constant__ AttnDecodeArgs a) {
+// One CTA per (head, row), kMergeSlices x 128 threads: thread (slice i, dim d)
+// folds blocks i, i + 8, i + 16, ... in order, all its loads issued ahead; the
+// eight slice sums are then added in slice order.  The fold depends only on
+// the row's position (its block count), never on the other rows of the call.
+__global__ void __launch_bounds__(kHeadDim* kMergeSlices) attn_merge_kernel(const __grid_constant__ AttnDecodeArgs a) {
+    constexpr int kT = kHeadDim * kMergeSlices;
     __shared__ float wts[1024];
-    __shared__ float red[kHeadDim / 32];
+    __shared__ float red[kT / 32];
+    __shared__ float so[kMergeSlices][kHeadDim];
+    __shared__ float sl[kMergeSlices];
     pdl_wait();
-    const int head = blockIdx.x, row = blockIdx.y, d = threadIdx.x;
+    pdl_trigger();
+    const int head = blockIdx.x, row = blockIdx.y, tid = threadIdx.x;
+    const int d = tid & (kHeadDim - 1), slice = tid / kHeadDim;
     const int s = row_stream(a.rows, row);
     const int pos = a.rows.pos0[s] + (row - a.rows.row_start[s]);
     const int nb = pos / kKB + 1;
     const size_t base = ((size_t)row * a.n_q + head) * a.max_blocks;
 
     float M = -INFINITY;
-    for (int b = d; b < nb; b += kHeadDim) M = fmaxf(M, a.pm[base + b]);
+    for (int b = tid; b < nb; b += kT) M = fmaxf(M, a.pm[base + b]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if ((d & 31) == 0) red[d >> 5] = M;
+    if ((tid & 31) == 0) red[tid >> 5] = M;
     __syncthreads();
-    M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < kT / 32; ++w) M = fmaxf(M, red[w]);
 
     float O = 0.f, L = 0.f;
     for (int c = 0; c < nb; c += 1024) {
         const int n = min(1024, nb - c);
         __syncthreads();
-        for (int b = d; b < n; b += kHeadDim) wts[b] = exp2f(a.pm[base + c + b] - M);
+        for (int b = tid; b < n; b += kT) wts[b] = exp2f(a.pm[base + c + b] - M);
         __syncthreads();
         const float* pl = a.pl + base + c;
         const float* po = a.po + (base + c) * kHeadDim + d;
-        int b = 0;
-        for (; b + 16 <= n; b += 16) {
-            float lv[16], ov[16];
+        int b = slice;
+        for (; b + 7 * kMergeSlices < n; b += 8 * kMergeSlices) {
+            float lv[8], ov[8];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                lv[u] = pl[b + u];
-                ov[u] = po[(size_t)(b + u) * kHeadDim];
+            for (int u = 0; u < 8; ++u) {
+                lv[u] = pl[b + u * kMergeSlices];
+                ov[u] = po[(size_t)(b + u * kMergeSlices) * kHeadDim];
             }
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                L = fmaf(lv[u], wts[b + u], L);
-                O = fmaf(ov[u], wts[b + u], O);
+            for (int u = 0; u < 8; ++u) {
+                L = fmaf(lv[u], wts[b + u * kMergeSlices], L);
+                O = fmaf(ov[u], wts[b + u * kMergeSlices], O);
             }
         }
-        for (; b < n; ++b) {
+        for (; b < n; b += kMergeSlices) {
             L = fmaf(pl[b], wts[b], L);
             O = fmaf(po[(size_t)b * kHeadDim], wts[b], O);
         }
     }
-    pdl_trigger();
-    a.out[(size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + d] = rn(O / L);
+    so[slice][d] = O;
+    if (d == 0) sl[slice] = L;
+    __syncthreads();
+    if (slice == 0) {
+        O = so[0][d];
+        L = sl[0];
+#pragma unroll
+        for (int i = 1; i < kMergeSlices; ++i) {
+            O += so[i][d];
+            L += sl[i];
+        }
+        a.out[(size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + d] = rn(O / L);
+    }
 }
 
 }  // namespace
@@ -356,7 +403,7 @@ cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t c2 = {};
     c2.gridDim = dim3(a.n_q, a.rows.n_rows);
-    c2.blockDim = dim3(kHeadDim);
+    c2.blockDim = dim3(kHeadDim * kMergeSlices);
     c2.stream = st;
     c2.attrs = attr;
     c2.numAttrs = pdl ? 1 : 0;

@@ -39,29 +39,23 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kKbPerStage = 8;                 // 8 x 64 columns per stage
 constexpr int kABytes = 16 * 64 * 2 * kKbPerStage;  // 16 rows x 512 bf16 = 16 KB
 
-template <int NT>
-struct Cfg {
-    static constexpr int kXBytes = 8 * NT * 128 * kKbPerStage;  // up to 8*NT rows x 512 bf16
-    static constexpr int kStage = kABytes + kXBytes;
-    static constexpr int kDepth = (200 * 1024 / kStage) < 8 ? (200 * 1024 / kStage) : 8;
-    static constexpr int kRed = kConsumerWarps * NT * 4 * 32 * 4;  // cross-warp sums
-    static constexpr int kSmem = 1024 + kDepth * kStage + kRed + 2 * kDepth * 8 + 64;
-};
+// Shared memory of one CTA: a ring of `depth` stages (16 KB of weights plus
+// the stage's activation rows, 1 KB per row) of up to 200 KB, the cross-warp
+// sums and the barriers; the fused-norm variant keeps its normalised rows
+// instead of per-stage activations.  (Rings of 128 KB and more stream at the
+// same rate; 104 KB loses about 3% at one row.)
+constexpr int kRing = 200 * 1024;
+constexpr int kRedBytes(int nt) { return kConsumerWarps * nt * 4 * 32 * 4; }
+constexpr int kRedNorm = 8 * 8 * 4;
 
-// Fused-norm variant (up to 8 activation rows): stages hold weights only; the
-// normalised rows live in shared memory for the whole kernel.
-struct NormCfg {
-    static constexpr int kBudget = 216 * 1024;
-    static constexpr int kRed = kConsumerWarps * 4 * 32 * 4;
-    static constexpr int kRedNorm = 8 * 8 * 4;
-    static int depth(int xn_bytes) {
-        int d = (kBudget - 1024 - xn_bytes - kRed - kRedNorm - 2 * 8 * 8 - 64) / kABytes;
-        return d < 8 ? d : 8;
-    }
-    static int smem(int depth, int xn_bytes) {
-        return 1024 + depth * kABytes + xn_bytes + kRed + kRedNorm + 2 * 8 * 8 + 64;
-    }
-};
+int ring_depth(int stage_bytes, int budget) {
+    int d = budget / stage_bytes;
+    return d < 2 ? 2 : d > 8 ? 8 : d;
+}
+int stage_bytes_of(int x_rows_box, bool norm) { return kABytes + (norm ? 0 : x_rows_box * 1024); }
+int smem_bytes(int nt, bool norm, int depth, int stage_bytes, int xn_bytes) {
+    return 1024 + depth * stage_bytes + xn_bytes + kRedBytes(nt) + (norm ? kRedNorm : 0) + 2 * depth * 8 + 64;
+}
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -137,12 +131,11 @@ __device__ __forceinline__ void load_weights(const MatvecTmaArgs& a, int t, int 
 // (with a.norm_w) into shared memory by the consumers; requires NT == 1.
 template <int NT, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_constant__ MatvecTmaArgs a) {
-    using C = Cfg<NT>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* base =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int depth = NORM ? a.depth : C::kDepth;
-    const int stage_bytes = NORM ? kABytes : C::kStage;
+    const int depth = a.depth;
+    const int stage_bytes = kABytes + (NORM ? 0 : a.x_rows_box * 1024);
     const int xn_bytes = NORM ? a.e.n_rows * a.e.K * 2 : 0;
     unsigned char* xn = base + depth * stage_bytes;  // NORM: [k-block][row][64], swizzled lines
     float* red = reinterpret_cast<float*>(xn + xn_bytes);
@@ -181,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
                 if (++ks == nst) { ks = 0; t += gridDim.x; }
             }
             pdl_wait();
+            pdl_trigger();
             if (!NORM)
                 for (int i = 0; i < n_pre; ++i)
                     tma_load_3d(base + i * stage_bytes + kABytes, &a.xmap, 0, 0, pre_ks[i] * kKbPerStage, &full[i], px);
@@ -202,12 +196,15 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
             if (*s_abort) __nanosleep(500000);
         } else {
             pdl_wait();
+            pdl_trigger();
         }
         return;
     }
 
     // ---------------- consumers ----------------
+    // the next kernel may launch once every CTA is past its dependency wait
     pdl_wait();
+    pdl_trigger();
     const int g = lane >> 2, tig = lane & 3;
     const int R = a.e.n_rows, xrows = a.x_rows_box;
     const uint32_t base_u = smem_u32(base);
@@ -299,7 +296,6 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
         }
         named_barrier(1, kConsumerWarps * 32);
     }
-    pdl_trigger();
 }
 
 template <int NT, bool NORM>
@@ -307,7 +303,8 @@ cudaError_t launch_nt(const MatvecTmaArgs& a, int grid, cudaStream_t st, bool pd
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = NORM ? NormCfg::smem(a.depth, a.e.n_rows * a.e.K * 2) : Cfg<NT>::kSmem;
+    cfg.dynamicSmemBytes =
+        smem_bytes(NT, NORM, a.depth, stage_bytes_of(a.x_rows_box, NORM), NORM ? a.e.n_rows * a.e.K * 2 : 0);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -330,32 +327,50 @@ int matvec_tma_tiles(const MatvecArgs& e) {
 }
 
 cudaError_t init_matvec_tma() {
+    const int mx = 227 * 1024;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  Cfg<1>::kSmem)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  Cfg<2>::kSmem)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  Cfg<4>::kSmem)) != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  Cfg<8>::kSmem)) != cudaSuccess) return e;
-    return cudaFuncSetAttribute(matvec_tma_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                NormCfg::kBudget);
+    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)))
+        return e;
+    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)))
+        return e;
+    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<4, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)))
+        return e;
+    if ((e = cudaFuncSetAttribute(matvec_tma_kernel<8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)))
+        return e;
+    return cudaFuncSetAttribute(matvec_tma_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
 }
 
-int matvec_norm_depth(int n_rows, int K) { return NormCfg::depth(n_rows * K * 2); }
+// Ring depth of a launch (the fused-norm variant when norm is set).
+int matvec_depth(int n_rows, int K, bool norm) {
+    const int sb = stage_bytes_of(matvec_tma_x_rows(n_rows), norm);
+    const int d = ring_depth(sb, kRing);
+    if (norm) {
+        // the normalised rows come on top of the ring: keep the CTA within 227 KB
+        const int xn = n_rows * K * 2;
+        int dd = d;
+        while (dd > 2 && smem_bytes(1, true, dd, sb, xn) > 227 * 1024) --dd;
+        return dd;
+    }
+    return d;
+}
 
-cudaError_t launch_matvec_tma(const MatvecTmaArgs& a, int grid, cudaStream_t st, bool pdl) {
+int matvec_norm_depth(int n_rows, int K) { return matvec_depth(n_rows, K, true); }
+
+cudaError_t launch_matvec_tma(const MatvecTmaArgs& a0, int grid, cudaStream_t st, bool pdl) {
+    MatvecTmaArgs a = a0;
     const int nt = matvec_tma_nt(a.e.n_rows);
     if (a.e.n_rows < 1 || a.e.n_rows > kMaxDecodeRows || a.kstages < 1 || a.tiles < 1 ||
         a.x_rows_box != matvec_tma_x_rows(a.e.n_rows) || a.e.K % 64 != 0 ||
         a.kstages != (a.e.K + 64 * kKbPerStage - 1) / (64 * kKbPerStage))
         return cudaErrorInvalidValue;
     if (grid > a.tiles) grid = a.tiles;
-    if (a.norm_w) {
-        if (nt != 1 || a.depth < 2 || a.depth > 8 || a.depth != NormCfg::depth(a.e.n_rows * a.e.K * 2) ||
-            a.e.K % 64 != 0)
-            return cudaErrorInvalidValue;
+    const bool norm = a.norm_w != nullptr;
+    a.depth = matvec_depth(a.e.n_rows, a.e.K, norm);
+    const int sb = stage_bytes_of(a.x_rows_box, norm);
+    if (smem_bytes(nt, norm, a.depth, sb, norm ? a.e.n_rows * a.e.K * 2 : 0) > 227 * 1024)
+        return cudaErrorInvalidValue;
+    if (norm) {
+        if (nt != 1) return cudaErrorInvalidValue;
         return launch_nt<1, true>(a, grid, st, pdl);
     }
     switch (nt) {

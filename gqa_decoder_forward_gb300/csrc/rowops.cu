@@ -37,9 +37,9 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const bf16* x, co
                                                               bf16* out) {
     __shared__ float red[kNormThreads / 32];
     pdl_wait();
+    pdl_trigger();
     const size_t row = blockIdx.x;
     rmsnorm_row(x + row * H, w, eps, H, out + row * H, red);
-    pdl_trigger();
 }
 
 __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const int32_t* ids, const bf16* embed, int vocab,
@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const int32
                                                                     int* status) {
     __shared__ float red[kNormThreads / 32];
     pdl_wait();
+    pdl_trigger();
     const size_t row = blockIdx.x;
     const int id = ids[row];
     bf16* hr = h + row * H;
@@ -61,7 +62,6 @@ __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const int32
     }
     __syncthreads();
     rmsnorm_row(hr, w, eps, H, xn + row * H, red);
-    pdl_trigger();
 }
 
 constexpr int kArgThreads = 1024;
@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kArgThreads) argmax_kernel(const bf16* logits,
     __shared__ int bi[kArgThreads / 32];
     __shared__ int bad_any;
     pdl_wait();
+    pdl_trigger();
     if (threadIdx.x == 0) bad_any = 0;
     __syncthreads();
     const bf16* row = logits + (size_t)blockIdx.x * V;
@@ -97,7 +98,6 @@ __global__ void __launch_bounds__(kArgThreads) argmax_kernel(const bf16* logits,
     const int warp = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) { bv[warp] = best; bi[warp] = idx; }
     __syncthreads();
-    pdl_trigger();
     if (threadIdx.x == 0) {
         float b = bv[0];
         int j = bi[0];
