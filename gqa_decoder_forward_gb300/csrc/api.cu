@@ -501,7 +501,7 @@ cudaError_t gemm_launch(tfl_model* m, const MatvecArgs& e, const CUtensorMap* am
     if (b1) g.bmap[1] = *b1;
     if (b2) g.bmap[2] = *b2;
     g.m_tiles = (e.n_rows + 127) / 128;
-    g.n_tiles = e.mode == MV_SWIGLU ? e.n_out / 64 : e.mode == MV_QKV_ROPE ? e.n_q + 2 * e.n_kv : e.n_out / 256;
+    g.n_tiles = gemm_n_tiles(e);
     g.kblocks = e.K / 64;
     g.status = m->status;
     return launch_gemm_tc(g, m->grid, st, pdl);
@@ -751,7 +751,7 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
                   encode_map(&x.d, m->wd[l], F, H, 16) &&
                   encode_map2d(&x.gq, m->wq[l], H, QD, 128) && encode_map2d(&x.gk, m->wk[l], H, KD, 128) &&
                   encode_map2d(&x.gv, m->wv[l], H, KD, 128) && encode_map2d(&x.go, m->wo[l], QD, H, 256) &&
-                  encode_map2d(&x.gg, m->wg[l], H, F, 64) && encode_map2d(&x.gu, m->wu[l], H, F, 64) &&
+                  encode_map2d(&x.gg, m->wg[l], H, F, 128) && encode_map2d(&x.gu, m->wu[l], H, F, 128) &&
                   encode_map2d(&x.gd, m->wd[l], F, H, 256);
         }
         okm = okm && encode_map(&m->lm_map, m->lm_head, H, cfg->vocab, 16);

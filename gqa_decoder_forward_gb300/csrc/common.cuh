@@ -125,6 +125,7 @@ struct GemmArgs {
 };
 cudaError_t init_gemm_tc();
 int gemm_tile_n(int mode);
+int gemm_n_tiles(const MatvecArgs& e);  // output tiles of a projection, -1 if the shape does not tile
 cudaError_t launch_gemm_tc(const GemmArgs& a, int grid, cudaStream_t st, bool pdl);
 
 cudaError_t launch_embed_rmsnorm(const int32_t* ids, const bf16* embed, int vocab, const bf16* w, float eps,

@@ -4,15 +4,15 @@
 // rows on the tensor-unit GEMM").  fp32 accumulation in tensor memory, one
 // rounding to bf16 per output.
 //
-// One CTA per SM, persistent over output tiles of 128 activation rows x N
-// weight rows (N = 256 for plain projections; 128 = one head for QKV, or 64
-// gate + 64 up rows for SwiGLU so that every pair an epilogue combines lands in
-// the same thread):
+// One CTA per SM, persistent over output tiles of 128 activation rows x 256
+// weight rows (256 output features; for QKV two heads of [q | k | v], for
+// SwiGLU 128 gate rows and the 128 up rows of the same features, so that every
+// pair an epilogue combines lands in the same thread):
 //   warp 0      TMA producer: per 64-wide k-block, the 128 x 64 activation box
 //               and the N x 64 weight box(es), 128-byte swizzled, into a ring
 //               of shared-memory stages;
 //   warp 1      allocates tensor memory; one thread issues tcgen05.mma
-//               (M = 128, N, K = 16; four per stage) into one of two
+//               (M = 128, N = 256, K = 16; four per stage) into one of two
 //               accumulators and commits each stage back to the producer;
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per thread),
 //               the op after the projection, bf16 stores; the accumulator is
@@ -43,6 +43,12 @@ struct GCfg {
 };
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// Global head index gh of [q heads | k heads | v heads] -> segment (0 q, 1 k, 2 v) and head.
+__device__ __forceinline__ void qkv_head(const MatvecArgs& e, int gh, int& seg, int& head) {
+    seg = gh < e.n_q ? 0 : (gh < e.n_q + e.n_kv ? 1 : 2);
+    head = gh - (seg == 0 ? 0 : seg == 1 ? e.n_q : e.n_q + e.n_kv);
+}
 
 template <int N>
 __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ GemmArgs a) {
@@ -100,14 +106,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     unsigned char* sB = sA + kABytes;
                     mbar_arrive_expect_tx(&full[stage], C::kStage);
                     tma_load_2d(sA, &a.amap, kb * 64, m * kTM, &full[stage], pa);
-                    if (a.e.mode == MV_SWIGLU) {
-                        tma_load_2d(sB, &a.bmap[0], kb * 64, n * 64, &full[stage], pb);
-                        tma_load_2d(sB + 64 * 128, &a.bmap[1], kb * 64, n * 64, &full[stage], pb);
-                    } else if (a.e.mode == MV_QKV_ROPE) {
-                        const int nq = a.e.n_q, nkv = a.e.n_kv;
-                        const int seg = n < nq ? 0 : (n < nq + nkv ? 1 : 2);
-                        const int head = n - (seg == 0 ? 0 : seg == 1 ? nq : nq + nkv);
-                        tma_load_2d(sB, &a.bmap[seg], kb * 64, head * kHeadDim, &full[stage], pb);
+                    if (a.e.mode == MV_SWIGLU) {  // 128 gate rows, then the 128 up rows of the same features
+                        tma_load_2d(sB, &a.bmap[0], kb * 64, n * 128, &full[stage], pb);
+                        tma_load_2d(sB + 128 * 128, &a.bmap[1], kb * 64, n * 128, &full[stage], pb);
+                    } else if (a.e.mode == MV_QKV_ROPE) {  // heads 2n and 2n+1 of [q heads | k heads | v heads]
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            int seg, head;
+                            qkv_head(a.e, 2 * n + hh, seg, head);
+                            tma_load_2d(sB + hh * 128 * 128, &a.bmap[seg], kb * 64, head * kHeadDim, &full[stage], pb);
+                        }
                     } else {
                         tma_load_2d(sB, &a.bmap[0], kb * 64, n * N, &full[stage], pb);
                     }
@@ -203,35 +211,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     }
                 }
             } else if (a.e.mode == MV_SWIGLU) {
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 8; ++c) {
                     float gv[16], uv[16];
                     __syncwarp();
                     tmem_ld16(acc + c * 16, gv);
-                    tmem_ld16(acc + 64 + c * 16, uv);
+                    tmem_ld16(acc + 128 + c * 16, uv);
                     if (!live) continue;
                     uint4 o[2];
                     bf16* oe = reinterpret_cast<bf16*>(o);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) oe[j] = rn(rbf(silu_f(rbf(gv[j]))) * rbf(uv[j]));
-                    uint4* yp = reinterpret_cast<uint4*>(a.e.y + (size_t)r * a.e.ldy + (size_t)n * 64 + c * 16);
+                    uint4* yp = reinterpret_cast<uint4*>(a.e.y + (size_t)r * a.e.ldy + (size_t)n * 128 + c * 16);
                     yp[0] = o[0];
                     yp[1] = o[1];
                 }
-            } else {  // MV_QKV_ROPE: n is the head (q heads, then k, then v)
-                const int nq = a.e.n_q, nkv = a.e.n_kv;
-                const int seg = n < nq ? 0 : (n < nq + nkv ? 1 : 2);
-                const int head = n - (seg == 0 ? 0 : seg == 1 ? nq : nq + nkv);
+            } else {  // MV_QKV_ROPE: heads 2n, 2n+1 of [q heads | k heads | v heads]
+              for (int hh = 0; hh < 2; ++hh) {
+                int seg, head;
+                qkv_head(a.e, 2 * n + hh, seg, head);
                 const int pos = a.e.rows.pos0[0] + r;
                 bf16* dst = nullptr;
                 if (live) {
                     dst = seg == 0 ? a.e.y + (size_t)r * a.e.ldy + (size_t)head * kHeadDim
-                                   : kv_row(a.e.rows.kv[0], a.e.layer, seg - 1, pos, nkv) + (size_t)head * kHeadDim;
+                                   : kv_row(a.e.rows.kv[0], a.e.layer, seg - 1, pos, a.e.n_kv) +
+                                         (size_t)head * kHeadDim;
                 }
+                const uint32_t acc_h = acc + (uint32_t)(hh * 128);
                 for (int c = 0; c < 4; ++c) {
                     float lo[16], hi[16];
                     __syncwarp();
-                    tmem_ld16(acc + c * 16, lo);
-                    tmem_ld16(acc + 64 + c * 16, hi);
+                    tmem_ld16(acc_h + c * 16, lo);
+                    tmem_ld16(acc_h + 64 + c * 16, hi);
                     if (!live) continue;
                     uint4 ol[2], oh[2];
                     bf16* ole = reinterpret_cast<bf16*>(ol);
@@ -257,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     ph[0] = oh[0];
                     ph[1] = oh[1];
                 }
+              }
             }
             tc_fence_before();
             __syncwarp();
@@ -298,25 +309,24 @@ cudaError_t launch_n(const GemmArgs& a, int grid, cudaStream_t st, bool pdl) {
 }  // namespace
 
 cudaError_t init_gemm_tc() {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         GCfg<128>::kSmem);
-    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(gemm_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, GCfg<256>::kSmem);
 }
 
-int gemm_tile_n(int mode) { return (mode == MV_STORE || mode == MV_RESIDUAL) ? 256 : 128; }
+int gemm_tile_n(int) { return 256; }
+
+int gemm_n_tiles(const MatvecArgs& e) {
+    if (e.mode == MV_SWIGLU) return e.n_out % 128 == 0 ? e.n_out / 128 : -1;
+    if (e.mode == MV_QKV_ROPE) return (e.n_q + 2 * e.n_kv) % 2 == 0 ? (e.n_q + 2 * e.n_kv) / 2 : -1;
+    return e.n_out % 256 == 0 ? e.n_out / 256 : -1;
+}
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, int grid, cudaStream_t st, bool pdl) {
-    if (a.e.n_rows < 1 || a.e.n_rows > a.m_tiles * kTM || a.kblocks < 1 || a.n_tiles < 1 || a.e.K != a.kblocks * 64)
-        return cudaErrorInvalidValue;
-    const int nt = a.e.mode == MV_SWIGLU ? a.e.n_out / 64
-                   : a.e.mode == MV_QKV_ROPE ? a.e.n_q + 2 * a.e.n_kv
-                                              : a.e.n_out / 256;
-    if (a.n_tiles != nt || (a.e.mode != MV_QKV_ROPE && a.e.n_out % (a.e.mode == MV_SWIGLU ? 64 : 256) != 0))
+    if (a.e.n_rows < 1 || a.e.n_rows > a.m_tiles * kTM || a.kblocks < 1 || a.n_tiles < 1 || a.e.K != a.kblocks * 64 ||
+        a.n_tiles != gemm_n_tiles(a.e))
         return cudaErrorInvalidValue;
     const int total = a.m_tiles * a.n_tiles;
     if (grid > total) grid = total;
-    return gemm_tile_n(a.e.mode) == 256 ? launch_n<256>(a, grid, st, pdl) : launch_n<128>(a, grid, st, pdl);
+    return launch_n<256>(a, grid, st, pdl);
 }
 
 }  // namespace tfl
