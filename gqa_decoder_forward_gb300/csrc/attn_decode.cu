@@ -26,24 +26,20 @@
 // row of P.  A row gives the same bits alone or beside other rows (one-row
 // steps == windows, solo == batched).
 #include "common.cuh"
+#include "attn_core.cuh"
+#include "tma.cuh"
 #include "warp_mma.cuh"
 
 namespace tfl {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kWarps = attn::kWarps;
 constexpr int kRB = 4;               // rows per CTA
-constexpr int kKB = kPage;           // keys per block
-constexpr int kMaxPairs = 32;        // kRB rows x up to 8 heads, two m16 tiles
-constexpr int kMergeSlices = 8;      // block slices of one merge CTA
-
-// Rows of 128 bf16 (256 bytes, 16 chunks of 16 bytes) with chunk c of row r
-// stored at chunk c ^ (r & 7): the eight rows an ldmatrix reads hit distinct
-// banks without padding.
-__device__ __forceinline__ int swz(int row, int col) {
-    return row * kHeadDim + (((col >> 3) ^ (row & 7)) << 3) + (col & 7);
-}
+constexpr int kKB = attn::kKB;
+constexpr int kMaxPairs = attn::kMaxPairs;
+constexpr int kMergeSlices = attn::kMergeSlices;
+using attn::swz;
 
 // 75,776 bytes: three CTAs per SM.  The softmax weights (hi and lo parts,
 // 2 x 32 x 128 bf16) reuse the key tile once the scores are computed.
@@ -58,10 +54,6 @@ struct Smem {
 using wm::cp_async16_zfill;
 using wm::cp_async_commit;
 using wm::cp_async_wait;
-using wm::ldsm_x4;
-using wm::ldsm_x4_t;
-using wm::mma16816;
-using wm::pack_bf16;
 
 // Locates row group z: stream s, first row (global index) r0, row count nr.
 __device__ __forceinline__ bool find_group(const RowMap& m, int z, int& s, int& r0, int& nr) {
@@ -142,149 +134,24 @@ __global__ void __launch_bounds__(kThreads, 3) attn_block_kernel(const __grid_co
     cp_async_wait<1>();  // the keys have landed; the values may still be in flight
     __syncthreads();
 
-    // ---- S = Q K^T: warp w owns keys 16w .. 16w+15 (two n8 tiles) ----
-    const float kScale = 0.12751743074640502f;  // log2(e) / sqrt(128)
-    float sc[2][2][4];  // [m tile][n tile][fragment]
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
-    {
-        const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8, mcol = (lane >> 4) * 8;     // A: matrices (r, k) quads
-        const int krow = (lane & 7) + (lane >> 4) * 8, kcol = ((lane >> 3) & 1) * 8;     // B: keys x dims
-#pragma unroll
-        for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-            uint32_t bk[4];
-            ldsm_x4(bk, &sm.k[swz(warp * 16 + krow, ks * 16 + kcol)]);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                if (mt < MT) {
-                    uint32_t aq[4];
-                    ldsm_x4(aq, &sm.q[swz(mt * 16 + mrow, ks * 16 + mcol)]);
-                    mma16816(sc[mt][0], aq, bk[0], bk[1]);
-                    mma16816(sc[mt][1], aq, bk[2], bk[3]);
-                }
-            }
-        }
-    }
-    // scale, mask, per-warp row maxima
-    float mx[2][2];  // [m tile][row half]
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int p = mt * 16 + gq + h * 8;
-            const int pos_row = p_first + (p < P ? p / G : 0);
-            float m = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = warp * 16 + nt * 8 + 2 * tig + e;
-                    const bool vis = p < P && t < nv && k0 + t <= pos_row;
-                    float& v = sc[mt][nt][h * 2 + e];
-                    v = vis ? v * kScale : -INFINITY;
-                    m = fmaxf(m, v);
-                }
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            mx[mt][h] = m;
-        }
-    }
-    if (tig == 0) {
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) sm.wmax[warp][mt * 16 + gq + h * 8] = mx[mt][h];
-    }
-    __syncthreads();
-    // block row maxima, weights, per-warp row sums, weights to shared memory
-    // (over the key tile, which no warp reads any more)
-    bf16* pw = sm.k;
-    float bmax[2][2];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int p = mt * 16 + gq + h * 8;
-            float m = sm.wmax[0][p];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) m = fmaxf(m, sm.wmax[w][p]);
-            bmax[mt][h] = m;
-            float l = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                float e0 = 0.f, e1 = 0.f;
-                if (m != -INFINITY) {
-                    e0 = exp2f(sc[mt][nt][h * 2 + 0] - m);
-                    e1 = exp2f(sc[mt][nt][h * 2 + 1] - m);
-                }
-                l += e0;
-                l += e1;
-                const bf16 h0 = rn(e0), h1 = rn(e1);
-                const bf16 l0 = rn(e0 - bf(h0)), l1 = rn(e1 - bf(h1));
-                const int t = warp * 16 + nt * 8 + 2 * tig;
-                *reinterpret_cast<uint32_t*>(&pw[swz(p, t)]) = pack_bf16(h0, h1);
-                *reinterpret_cast<uint32_t*>(&pw[kMaxPairs * kHeadDim + swz(p, t)]) = pack_bf16(l0, l1);
-            }
-            l += __shfl_xor_sync(0xffffffffu, l, 1);
-            l += __shfl_xor_sync(0xffffffffu, l, 2);
-            if (tig == 0) sm.wsum[warp][p] = l;
-        }
-    }
-    cp_async_wait<0>();  // the values
-    __syncthreads();
-
-    // ---- O = P V: warp w owns dims 16w .. 16w+15 (two n8 tiles) ----
-    float oc[2][2][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) oc[mt][nt][0] = oc[mt][nt][1] = oc[mt][nt][2] = oc[mt][nt][3] = 0.f;
-    {
-        const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8, mcol = (lane >> 4) * 8;  // A: pairs x keys
-        const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8, vcol = (lane >> 4) * 8;  // B (trans): keys x dims
-#pragma unroll 2
-        for (int ks = 0; ks < kKB / 16; ++ks) {
-            uint32_t bv[4];
-            ldsm_x4_t(bv, &sm.v[swz(ks * 16 + vrow, warp * 16 + vcol)]);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                if (mt < MT) {
-#pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        uint32_t ap[4];
-                        ldsm_x4(ap, &pw[part * kMaxPairs * kHeadDim + swz(mt * 16 + mrow, ks * 16 + mcol)]);
-                        mma16816(oc[mt][0], ap, bv[0], bv[1]);
-                        mma16816(oc[mt][1], ap, bv[2], bv[3]);
-                    }
-                }
-            }
-        }
-    }
-
-    // ---- partials: o (unnormalised), m, l per (row, head) ----
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int p = mt * 16 + gq + h * 8;
-            if (mt < MT && p < P) {
-                const int row = r0 + p / G, head = g * G + p % G;
-                const size_t idx = ((size_t)row * a.n_q + head) * a.max_blocks + b;
-                float* po = a.po + idx * kHeadDim + warp * 16 + 2 * tig;
-                *reinterpret_cast<float2*>(po) = make_float2(oc[mt][0][h * 2 + 0], oc[mt][0][h * 2 + 1]);
-                *reinterpret_cast<float2*>(po + 8) = make_float2(oc[mt][1][h * 2 + 0], oc[mt][1][h * 2 + 1]);
-                if (warp == 0 && tig == 0) {
-                    float l = sm.wsum[0][p];
-#pragma unroll
-                    for (int w = 1; w < kWarps; ++w) l += sm.wsum[w][p];
-                    a.pm[idx] = bmax[mt][h];
-                    a.pl[idx] = l;
-                }
-            }
-        }
-    }
+    attn::BlockGeom bg;
+    bg.b = b;
+    bg.g = g;
+    bg.r0 = r0;
+    bg.P = P;
+    bg.MT = MT;
+    bg.k0 = k0;
+    bg.nv = nv;
+    bg.p_first = p_first;
+    const uint32_t k_u = smem_u32(sm.k), v_u = smem_u32(sm.v);
+    attn::block_partial<G>(
+        a, bg, smem_u32(sm.q), k_u, sm.wmax, sm.wsum,
+        [&](int row, int col) { return k_u + 2u * swz(row, col); },
+        [&](int row, int col) { return v_u + 2u * swz(row, col); }, [] { __syncthreads(); },
+        [] {
+            cp_async_wait<0>();  // the values
+            __syncthreads();
+        });
 }
 
 // One CTA per (head, row), kMergeSlices x 128 threads: thread (slice i, dim d)
@@ -299,63 +166,7 @@ __global__ void __launch_bounds__(kHeadDim* kMergeSlices) attn_merge_kernel(cons
     __shared__ float sl[kMergeSlices];
     pdl_wait();
     pdl_trigger();
-    const int head = blockIdx.x, row = blockIdx.y, tid = threadIdx.x;
-    const int d = tid & (kHeadDim - 1), slice = tid / kHeadDim;
-    const int s = row_stream(a.rows, row);
-    const int pos = a.rows.pos0[s] + (row - a.rows.row_start[s]);
-    const int nb = pos / kKB + 1;
-    const size_t base = ((size_t)row * a.n_q + head) * a.max_blocks;
-
-    float M = -INFINITY;
-    for (int b = tid; b < nb; b += kT) M = fmaxf(M, a.pm[base + b]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if ((tid & 31) == 0) red[tid >> 5] = M;
-    __syncthreads();
-    M = red[0];
-#pragma unroll
-    for (int w = 1; w < kT / 32; ++w) M = fmaxf(M, red[w]);
-
-    float O = 0.f, L = 0.f;
-    for (int c = 0; c < nb; c += 1024) {
-        const int n = min(1024, nb - c);
-        __syncthreads();
-        for (int b = tid; b < n; b += kT) wts[b] = exp2f(a.pm[base + c + b] - M);
-        __syncthreads();
-        const float* pl = a.pl + base + c;
-        const float* po = a.po + (base + c) * kHeadDim + d;
-        int b = slice;
-        for (; b + 7 * kMergeSlices < n; b += 8 * kMergeSlices) {
-            float lv[8], ov[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                lv[u] = pl[b + u * kMergeSlices];
-                ov[u] = po[(size_t)(b + u * kMergeSlices) * kHeadDim];
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                L = fmaf(lv[u], wts[b + u * kMergeSlices], L);
-                O = fmaf(ov[u], wts[b + u * kMergeSlices], O);
-            }
-        }
-        for (; b < n; b += kMergeSlices) {
-            L = fmaf(pl[b], wts[b], L);
-            O = fmaf(po[(size_t)b * kHeadDim], wts[b], O);
-        }
-    }
-    so[slice][d] = O;
-    if (d == 0) sl[slice] = L;
-    __syncthreads();
-    if (slice == 0) {
-        O = so[0][d];
-        L = sl[0];
-#pragma unroll
-        for (int i = 1; i < kMergeSlices; ++i) {
-            O += so[i][d];
-            L += sl[i];
-        }
-        a.out[(size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + d] = rn(O / L);
-    }
+    attn::merge<kT>(a, blockIdx.y, blockIdx.x, threadIdx.x, wts, red, so, sl, [] { __syncthreads(); });
 }
 
 }  // namespace

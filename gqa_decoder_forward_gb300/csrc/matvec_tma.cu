@@ -27,17 +27,16 @@
 #include <cuda.h>
 
 #include "common.cuh"
-#include "matvec_epilogue.cuh"
-#include "rmsnorm_row.cuh"
+#include "matvec_core.cuh"
 #include "tma.cuh"
 
 namespace tfl {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+using mvc::kABytes;
+using mvc::kConsumerWarps;
+using mvc::kKbPerStage;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kKbPerStage = 8;                 // 8 x 64 columns per stage
-constexpr int kABytes = 16 * 64 * 2 * kKbPerStage;  // 16 rows x 512 bf16 = 16 KB
 
 // Shared memory of one CTA: a ring of `depth` stages (16 KB of weights plus
 // the stage's activation rows, 1 KB per row) of up to 200 KB, the cross-warp
@@ -55,76 +54,6 @@ int ring_depth(int stage_bytes, int budget) {
 int stage_bytes_of(int x_rows_box, bool norm) { return kABytes + (norm ? 0 : x_rows_box * 1024); }
 int smem_bytes(int nt, bool norm, int depth, int stage_bytes, int xn_bytes) {
     return 1024 + depth * stage_bytes + xn_bytes + kRedBytes(nt) + (norm ? kRedNorm : 0) + 2 * depth * 8 + 64;
-}
-
-__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 r;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
-    return r;
-}
-
-// The two 16-byte chunks (tig and tig+4) of 128-byte line `line` of a tile
-// written by TMA with 128-byte swizzling (chunk c of line l sits at chunk
-// c ^ (l mod 8)).  Lines with odd (l mod 8) read the upper chunk first, so each
-// 8-lane phase of a warp touches 8 distinct bank groups.
-__device__ __forceinline__ void line_chunks(uint32_t tile, int line, int tig, uint4& c0, uint4& c1) {
-    const int sw = line & 7, odd = line & 1;
-    const uint32_t row = tile + line * 128;
-    uint4 a = lds128(row + (((tig + 4 * odd) ^ sw) << 4));
-    uint4 b = lds128(row + (((tig + 4 * (1 - odd)) ^ sw) << 4));
-    c0 = odd ? b : a;
-    c1 = odd ? a : b;
-}
-
-__device__ __forceinline__ mv::TileRows tile_info(const MatvecArgs& e, int t) {
-    mv::TileRows r;
-    r.lo = r.hi = nullptr;
-    r.seg = 0;
-    r.head = 0;
-    if (e.mode == MV_SWIGLU) {
-        r.j0 = t * 8;
-    } else if (e.mode == MV_QKV_ROPE) {
-        const int tq = e.n_q * 8, tk = e.n_kv * 8;
-        int u;
-        if (t < tq) { r.seg = 0; u = t; }
-        else if (t < tq + tk) { r.seg = 1; u = t - tq; }
-        else { r.seg = 2; u = t - tq - tk; }
-        r.head = u / 8;
-        r.j0 = (u % 8) * 8;
-    } else {
-        r.j0 = t * 16;
-    }
-    return r;
-}
-
-// TMA loads of the 16 weight rows of tile t, k-blocks kb..kb+7, into sA:
-// layout [k-block][16 rows][64], lo rows first.
-__device__ __forceinline__ void load_weights(const MatvecTmaArgs& a, int t, int kb, unsigned char* sA,
-                                             uint64_t* bar, uint64_t pol) {
-    if (a.e.mode == MV_STORE || a.e.mode == MV_RESIDUAL) {
-        tma_load_3d(sA, &a.wmap[0], 0, t * 16, kb, bar, pol);
-    } else if (a.e.mode == MV_SWIGLU) {
-        tma_load_3d(sA, &a.wmap[0], 0, t * 8, kb, bar, pol);          // gate rows (box of 8 rows)
-        tma_load_3d(sA + kABytes / 2, &a.wmap[1], 0, t * 8, kb, bar, pol);  // up rows
-    } else {
-        const int tq = a.e.n_q * 8, tk = a.e.n_kv * 8;
-        int seg, u;
-        if (t < tq) { seg = 0; u = t; }
-        else if (t < tq + tk) { seg = 1; u = t - tq; }
-        else { seg = 2; u = t - tq - tk; }
-        const int row = (u / 8) * kHeadDim + (u % 8) * 8;
-        tma_load_3d(sA, &a.wmap[seg], 0, row, kb, bar, pol);
-        tma_load_3d(sA + kABytes / 2, &a.wmap[seg], 0, row + 64, kb, bar, pol);
-    }
 }
 
 // NORM: the activation rows are the residual stream a.e.x and are normalised
@@ -169,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
             int n_pre = 0;
             while (n_pre < depth && t < tiles) {
                 mbar_arrive_expect_tx(&full[n_pre], stage_tx);
-                load_weights(a, t, ks * kKbPerStage, base + n_pre * stage_bytes, &full[n_pre], pw);
+                mvc::load_weights(a.e, a.wmap, t, ks * kKbPerStage, base + n_pre * stage_bytes, &full[n_pre], pw);
                 pre_ks[n_pre++] = ks;
                 if (++ks == nst) { ks = 0; t += gridDim.x; }
             }
@@ -187,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
                 }
                 unsigned char* sA = base + stage * stage_bytes;
                 mbar_arrive_expect_tx(&full[stage], stage_tx);
-                load_weights(a, t, ks * kKbPerStage, sA, &full[stage], pw);
+                mvc::load_weights(a.e, a.wmap, t, ks * kKbPerStage, sA, &full[stage], pw);
                 if (!NORM) tma_load_3d(sA + kABytes, &a.xmap, 0, 0, ks * kKbPerStage, &full[stage], px);
                 if (++stage == depth) { stage = 0; phase ^= 1u; }
                 if (++ks == nst) { ks = 0; t += gridDim.x; }
@@ -205,96 +134,24 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
     // the next kernel may launch once every CTA is past its dependency wait
     pdl_wait();
     pdl_trigger();
-    const int g = lane >> 2, tig = lane & 3;
+    const int tig = lane & 3;
     const int R = a.e.n_rows, xrows = a.x_rows_box;
     const uint32_t base_u = smem_u32(base);
     const uint32_t xn_u = smem_u32(xn);
     const int kblocks = a.e.K / 64;
-    if (NORM) {
-        // the rows' RMSNorm, with the same arithmetic as the standalone norm kernel,
-        // into [k-block][row][64] lines (chunk c of line l at c ^ (l mod 8))
-        const int K = a.e.K, tid = threadIdx.x;
-        for (int r = 0; r < R; ++r) {
-            const bf16* hr = a.e.x + (size_t)r * K;
-            const float rinv = rms_inv(hr, K, a.eps, tid, red_norm + r * 8, [] { named_barrier(1, kConsumerWarps * 32); });
-            for (int i = tid * 8; i < K; i += kNormThreads * 8) {
-                const uint4 hv = *reinterpret_cast<const uint4*>(hr + i);
-                const uint4 wv = __ldg(reinterpret_cast<const uint4*>(a.norm_w + i));
-                const bf16* he = reinterpret_cast<const bf16*>(&hv);
-                const bf16* we = reinterpret_cast<const bf16*>(&wv);
-                uint4 o;
-                bf16* oe = reinterpret_cast<bf16*>(&o);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) oe[k] = rms_apply(he[k], we[k], rinv);
-                const int line = (i >> 6) * R + r, c = (i & 63) >> 3;
-                asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xn_u + line * 128 + ((c ^ (line & 7)) << 4)),
-                             "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
-                             : "memory");
-            }
-        }
-        named_barrier(1, kConsumerWarps * 32);
-    }
-    // line of this warp's lo / hi weight row inside a stage: [k-block][16 rows]
-    // for STORE/RESIDUAL; [k-block][8 lo rows] then [k-block][8 hi rows] otherwise
-    const bool two_boxes = a.e.mode == MV_SWIGLU || a.e.mode == MV_QKV_ROPE;
-    const int line_lo = two_boxes ? warp * 8 + g : warp * 16 + g;
-    const int line_hi = two_boxes ? (kABytes / 2) / 128 + warp * 8 + g : warp * 16 + 8 + g;
+    const mvc::NamedBar1 bar;
+    // NORM: the rows' RMSNorm, with the same arithmetic as the standalone norm
+    // kernel, into [k-block][row][64] lines
+    if (NORM) mvc::rows_to_lines(a.e.x, a.norm_w, a.eps, R, a.e.K, xn_u, red_norm, bar);
     int stage = 0;
     uint32_t phase = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-        float acc[NT][4];
-#pragma unroll
-        for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-        for (int ks = 0; ks < nst; ++ks) {
-            // after an abort every consumer keeps walking the loops (no more waits,
-            // no early return) so that all of them reach the named barriers below
-            if (!*s_abort && !mbar_wait(&full[stage], phase, a.status)) *s_abort = 1;
-            const uint32_t sA = base_u + stage * stage_bytes;
-            const uint32_t sX = sA + kABytes;
-            const int kb = ks * kKbPerStage + warp;  // this warp's k-block
-            uint4 l0, l1, h0, h1;
-            line_chunks(sA, line_lo, tig, l0, l1);
-            line_chunks(sA, line_hi, tig, h0, h1);
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const int xr = n * 8 + g;  // activation row of this lane's B fragment
-                uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
-                if (NORM) {
-                    if (xr < R && kb < kblocks) line_chunks(xn_u, kb * R + xr, tig, x0, x1);
-                } else if (xr < xrows) {
-                    line_chunks(sX, warp * xrows + xr, tig, x0, x1);
-                }
-                mma16816(acc[n], l0.x, h0.x, l0.y, h0.y, x0.x, x0.y);
-                mma16816(acc[n], l0.z, h0.z, l0.w, h0.w, x0.z, x0.w);
-                mma16816(acc[n], l1.x, h1.x, l1.y, h1.y, x1.x, x1.y);
-                mma16816(acc[n], l1.z, h1.z, l1.w, h1.w, x1.z, x1.w);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == depth) { stage = 0; phase ^= 1u; }
-        }
-        // fixed-order sum over the eight warps, then the epilogue
-#pragma unroll
-        for (int n = 0; n < NT; ++n)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) red[((warp * NT + n) * 4 + i) * 32 + lane] = acc[n][i];
-        named_barrier(1, kConsumerWarps * 32);
-        const mv::TileRows tr = tile_info(a.e, t);
-        for (int n = warp; n < NT; n += kConsumerWarps) {
-            float v[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float s = red[((0 * NT + n) * 4 + i) * 32 + lane];
-#pragma unroll
-                for (int w = 1; w < kConsumerWarps; ++w) s += red[((w * NT + n) * 4 + i) * 32 + lane];
-                v[i] = s;
-            }
-            // c0 = (lo g, row 2tig), c1 = (lo g, row 2tig+1), c2 = (hi g, row 2tig), c3 = (hi g, row 2tig+1)
-            const int r0 = n * 8 + 2 * tig;
-            if (r0 < R) mv::epilogue(a.e, tr, g, r0, v[0], v[2]);
-            if (r0 + 1 < R) mv::epilogue(a.e, tr, g, r0 + 1, v[1], v[3]);
-        }
-        named_barrier(1, kConsumerWarps * 32);
+        if (NORM)
+            mvc::consume_tile<NT>(a.e, t, nst, R, base_u, stage_bytes, depth, stage, phase, full, empty, red, s_abort,
+                                  a.status, mvc::XFromLines{xn_u, R, kblocks, tig}, bar);
+        else
+            mvc::consume_tile<NT>(a.e, t, nst, R, base_u, stage_bytes, depth, stage, phase, full, empty, red, s_abort,
+                                  a.status, mvc::XFromStage{xrows, warp, tig}, bar);
     }
 }
 
