@@ -90,7 +90,7 @@ int qualify(const tfl_config* c) {
 
 // Workspace layout (byte offsets, 256-byte aligned regions).
 struct Layout {
-    size_t h, xn, q, ao, act, pm, pl, po, cos_t, sin_t, status, total;
+    size_t h, xn, q, ao, act, pm, pl, po, cos_t, sin_t, status, wmaps, norms, sync, zero, total;
     int max_blocks;
 };
 
@@ -118,6 +118,12 @@ Layout layout(const tfl_config* c) {
     L.cos_t = take((size_t)c->max_context * 64 * 2);
     L.sin_t = take((size_t)c->max_context * 64 * 2);
     L.status = take(256);
+    // the decode-step kernel's tables: every projection's TMA descriptor, the
+    // norm weight pointers, the grid barrier words and a zero row
+    L.wmaps = take(((size_t)c->layers * 7 + 1) * sizeof(CUtensorMap));
+    L.norms = take((size_t)c->layers * 2 * sizeof(void*));
+    L.sync = take(256);
+    L.zero = take((size_t)c->hidden * 2);
     L.total = off;
     return L;
 }
@@ -186,6 +192,22 @@ bool encode_map2d(CUtensorMap* m, const void* ptr, uint64_t K, uint64_t rows, ui
     return r == CUDA_SUCCESS;
 }
 
+// A 3-D bf16 tensor map over a KV cache's pages, viewed as rows of n_kv x 128
+// (a row = one position of one (layer, K or V) page), boxes of 128 rows x one
+// head x 64 dims with 128-byte swizzle: the key or value tile of one block.
+bool encode_kv_map(CUtensorMap* m, const void* pages, int n_kv, uint64_t rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn || ((uintptr_t)pages & 15u)) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)n_kv, rows};
+    cuuint64_t strides[2] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)n_kv * kHeadDim * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kPage};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pages), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Index of the activation-row box for a call of `rows` rows: 1..8 -> 0..7,
 // 16 -> 8, 32 -> 9, 64 -> 10.
 int xbox_index(int rows) {
@@ -204,13 +226,13 @@ constexpr int kMaxFusedNormRows = 8;
 // Kernel families timed by tfl_profile (names in tfl_profile_kind).
 enum Kind {
     K_EMBED, K_NORM, K_QKV, K_ATTN, K_MERGE, K_O, K_GATEUP, K_DOWN, K_LMHEAD, K_ARGMAX,
-    K_GQKV, K_GO, K_GGATEUP, K_GDOWN, K_PATTN, K_COUNT
+    K_GQKV, K_GO, K_GGATEUP, K_GDOWN, K_PATTN, K_STEP, K_COUNT
 };
 const char* const kKindName[K_COUNT] = {"embed_rmsnorm", "rmsnorm", "matvec_qkv_rope", "attn_decode_block",
                                         "attn_decode_merge", "matvec_o_residual", "matvec_gate_up_swiglu",
                                         "matvec_down_residual", "matvec_lm_head", "argmax",
                                         "gemm_qkv_rope", "gemm_o_residual", "gemm_gate_up_swiglu",
-                                        "gemm_down_residual", "attn_prefill"};
+                                        "gemm_down_residual", "attn_prefill", "decode_step_persistent"};
 
 struct Mark {
     int kind;
@@ -226,6 +248,11 @@ struct tfl_model {
     bf16 *h, *xn, *q, *ao, *act, *cos_t, *sin_t;
     float *pm, *pl, *po;
     int* status;
+    CUtensorMap* d_wmaps;   // workspace copy of the decode matvec descriptors
+    const bf16** d_norms;   // workspace copy of the norm weight pointers
+    unsigned* sync;
+    bf16* zero_row;
+    bool persistent = true; // decode steps of <= kStepMaxRows rows as one launch
     bool pdl;
     // TMA descriptors of every projection and of the activation buffers
     struct LayerMaps {
@@ -285,6 +312,7 @@ struct tfl_kv {
     int length;
     int* table;
     bf16* pages;
+    CUtensorMap kvmap;  // 3-D over the pages: (128 dims, n_kv heads, rows), boxes of 128 rows x 64 dims
 };
 
 namespace {
@@ -471,6 +499,44 @@ int check_stream_kvs(tfl_model* m, tfl_kv* const* kvs, int n_streams, const int*
     return TFL_OK;
 }
 
+// A whole decode step of at most kStepMaxRows rows as one cooperative launch.
+int run_step_persistent(tfl_model* m, tfl_kv* const* kvs, const RowMap& rm, const int32_t* ids, void* logits,
+                        cudaStream_t st) {
+    const tfl_config& c = m->cfg;
+    StepArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.layers = c.layers;
+    a.H = c.hidden;
+    a.n_q = c.n_q;
+    a.n_kv = c.n_kv;
+    a.F = c.ffn;
+    a.V = c.vocab;
+    a.max_blocks = m->L.max_blocks;
+    a.eps = c.rms_eps;
+    a.wmaps = m->d_wmaps;
+    a.norms = m->d_norms;
+    a.final_norm = m->final_norm;
+    a.embed = m->embed;
+    a.zero_row = m->zero_row;
+    a.h = m->h;
+    a.q = m->q;
+    a.ao = m->ao;
+    a.act = m->act;
+    a.pm = m->pm;
+    a.pl = m->pl;
+    a.po = m->po;
+    a.cos_t = m->cos_t;
+    a.sin_t = m->sin_t;
+    a.status = m->status;
+    a.sync = m->sync;
+    a.ids = ids;
+    a.logits = (bf16*)logits;
+    a.rows = rm;
+    for (int s = 0; s < rm.n_streams; ++s) a.kvmap[s] = kvs[s]->kvmap;
+    LAUNCH(m, K_STEP, st, launch_step_persistent(a, m->grid, st));
+    return TFL_OK;
+}
+
 int decode_common(tfl_model* m, tfl_kv* const* kvs, int n_streams, const int* rows, const int32_t* ids,
                   const void* h_in, void* logits, void* h_out, cudaStream_t st) {
     RowMap rm;
@@ -479,6 +545,12 @@ int decode_common(tfl_model* m, tfl_kv* const* kvs, int n_streams, const int* ro
     for (int s = 0; s < n_streams; ++s)
         if (kvs[s]->length + rows[s] > m->cfg.max_context)
             return fail(TFL_E_CAPACITY, "stream %d passes the model's max_context %d", s, m->cfg.max_context);
+    if (m->persistent && ids && logits && !h_out && rm.n_rows <= kStepMaxRows) {
+        e = run_step_persistent(m, kvs, rm, ids, logits, st);
+        if (e) return e;
+        for (int s = 0; s < n_streams; ++s) kvs[s]->length += rows[s];
+        return ok();
+    }
     e = run_layers(m, rm, ids, h_in, st);
     if (e) return e;
     if (h_out) CK(cudaMemcpyAsync(h_out, m->h, (size_t)rm.n_rows * m->cfg.hidden * 2, cudaMemcpyDeviceToDevice, st));
@@ -735,6 +807,10 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
     m->cos_t = (bf16*)(m->ws + L.cos_t);
     m->sin_t = (bf16*)(m->ws + L.sin_t);
     m->status = (int*)(m->ws + L.status);
+    m->d_wmaps = (CUtensorMap*)(m->ws + L.wmaps);
+    m->d_norms = (const bf16**)(m->ws + L.norms);
+    m->sync = (unsigned*)(m->ws + L.sync);
+    m->zero_row = (bf16*)(m->ws + L.zero);
     m->pdl = true;
 
     // projections: TMA descriptors of every weight matrix and activation buffer
@@ -766,6 +842,25 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
         if (okm) ce0 = init_matvec_tma();
         if (okm && ce0 == cudaSuccess) ce0 = init_gemm_tc();
         if (okm && ce0 == cudaSuccess) ce0 = init_attn_prefill();
+        if (okm && ce0 == cudaSuccess) ce0 = init_step_persistent();
+        if (okm && ce0 == cudaSuccess) {
+            // device copies for the decode-step kernel: [layer][q k v o gate up down], lm_head; norms
+            std::vector<CUtensorMap> dm((size_t)cfg->layers * 7 + 1);
+            std::vector<const bf16*> dn((size_t)cfg->layers * 2);
+            for (int l = 0; l < cfg->layers; ++l) {
+                const tfl_model::LayerMaps& x = m->wmaps[l];
+                const CUtensorMap seven[7] = {x.q, x.k, x.v, x.o, x.g, x.u, x.d};
+                for (int j = 0; j < 7; ++j) dm[(size_t)l * 7 + j] = seven[j];
+                dn[(size_t)l * 2] = m->attn_norm[l];
+                dn[(size_t)l * 2 + 1] = m->ffn_norm[l];
+            }
+            dm.back() = m->lm_map;
+            ce0 = cudaMemcpy(m->d_wmaps, dm.data(), dm.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
+            if (ce0 == cudaSuccess)
+                ce0 = cudaMemcpy(m->d_norms, dn.data(), dn.size() * sizeof(void*), cudaMemcpyHostToDevice);
+            if (ce0 == cudaSuccess) ce0 = cudaMemset(m->zero_row, 0, (size_t)cfg->hidden * 2);
+            if (ce0 == cudaSuccess) ce0 = cudaMemset(m->sync, 0, 256);
+        }
         if (!okm || ce0 != cudaSuccess) {
             delete m;
             return fail(TFL_E_CUDA, "building TMA descriptors failed%s%s", ce0 ? ": " : "",
@@ -788,6 +883,12 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
 }
 
 void tfl_free(tfl_model* m) { delete m; }
+
+int tfl_set_persistent(tfl_model* m, int enable) {
+    if (!m) return fail(TFL_E_ARG, "NULL model");
+    m->persistent = enable != 0;
+    return ok();
+}
 
 size_t tfl_kv_bytes(const tfl_config* cfg, int max_positions) {
     if (!cfg || max_positions < 1 || cfg->n_kv < 1 || cfg->layers < 1) return 0;
@@ -813,6 +914,11 @@ int tfl_kv_alloc(tfl_model* m, int max_positions, void* dev_buf, size_t bytes, t
     kv->length = 0;
     kv->table = (int*)dev_buf;
     kv->pages = (bf16*)((char*)dev_buf + kv_table_bytes(kv->n_pages));
+    if (!encode_kv_map(&kv->kvmap, kv->pages, m->cfg.n_kv,
+                       (uint64_t)m->cfg.layers * 2 * (uint64_t)kv->n_pages * kPage)) {
+        delete kv;
+        return fail(TFL_E_CUDA, "building the KV tensor map failed");
+    }
     std::vector<int> ident(kv->n_pages);
     for (int i = 0; i < kv->n_pages; ++i) ident[i] = i;
     cudaError_t ce = cudaMemcpy(kv->table, ident.data(), ident.size() * 4, cudaMemcpyHostToDevice);

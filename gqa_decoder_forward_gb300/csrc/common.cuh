@@ -159,6 +159,31 @@ struct AttnPrefillArgs {
 cudaError_t init_attn_prefill();
 cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t st, bool pdl);
 
+// One whole decode step (embedding, every layer, final norm and lm_head) of at
+// most kStepMaxRows rows as one cooperative launch (step_persistent.cu).
+constexpr int kStepMaxRows = 2;
+struct StepArgs {
+    int layers, H, n_q, n_kv, F, V, max_blocks;
+    float eps;
+    const CUtensorMap* wmaps;   // device: [layers][7] (q, k, v, o, gate, up, down), then lm_head
+    const bf16* const* norms;   // device: [layers][2] (attention norm, FFN norm)
+    const bf16* final_norm;
+    const bf16* embed;
+    const bf16* zero_row;       // H zeros (the row of an out-of-range id)
+    bf16 *h, *q, *ao, *act;
+    float *pm, *pl, *po;
+    const bf16 *cos_t, *sin_t;
+    int* status;
+    unsigned* sync;             // [0] grid barrier counter (zero at launch), [1] abort flag
+    const int32_t* ids;         // device, n_rows
+    bf16* logits;               // device [n_rows][V]
+    RowMap rows;
+    CUtensorMap kvmap[kStepMaxRows];  // per stream: 3-D map over the cache pages (128 dims, n_kv, rows)
+};
+int step_smem_bytes();
+cudaError_t init_step_persistent();
+cudaError_t launch_step_persistent(const StepArgs& a, int grid, cudaStream_t st);
+
 cudaError_t launch_argmax(const bf16* logits, int n_rows, int V, int32_t* ids, int* status, cudaStream_t st,
                           bool pdl);
 

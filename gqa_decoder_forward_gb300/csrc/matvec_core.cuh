@@ -179,16 +179,17 @@ __device__ __forceinline__ void consume_tile(const MatvecArgs& e, int t, int nst
     bar();
 }
 
-// Activation rows (R rows of K bf16, optionally RMSNormed with w) into shared
-// lines [k-block][row][64] (line l = kb * R + r, chunk c of line l at chunk
-// c ^ (l mod 8)), by the 256 consumer threads.  The norm has the exact
-// arithmetic of the standalone norm kernel.  red_norm: 8 floats per row.
-template <class Bar>
-__device__ __forceinline__ void rows_to_lines(const bf16* x, const bf16* norm_w, float eps, int R, int K,
-                                              uint32_t xs_u, float* red_norm, Bar bar) {
+// Activation rows (R rows of K bf16, row r at row(r), optionally RMSNormed
+// with norm_w) into shared lines [k-block][row][64] (line l = kb * R + r, chunk
+// c of line l at chunk c ^ (l mod 8)), by the 256 consumer threads.  The norm
+// has the exact arithmetic of the standalone norm kernel.  red_norm: 8 floats
+// per row.
+template <class RowPtr, class Bar>
+__device__ __forceinline__ void rows_to_lines(RowPtr row, const bf16* norm_w, float eps, int R, int K, uint32_t xs_u,
+                                              float* red_norm, Bar bar) {
     const int tid = threadIdx.x;
     for (int r = 0; r < R; ++r) {
-        const bf16* hr = x + (size_t)r * K;
+        const bf16* hr = row(r);
         const float rinv = norm_w ? rms_inv(hr, K, eps, tid, red_norm + r * 8, bar) : 0.f;
         for (int i = tid * 8; i < K; i += kNormThreads * 8) {
             uint4 o = *reinterpret_cast<const uint4*>(hr + i);

@@ -142,7 +142,9 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
     const mvc::NamedBar1 bar;
     // NORM: the rows' RMSNorm, with the same arithmetic as the standalone norm
     // kernel, into [k-block][row][64] lines
-    if (NORM) mvc::rows_to_lines(a.e.x, a.norm_w, a.eps, R, a.e.K, xn_u, red_norm, bar);
+    if (NORM)
+        mvc::rows_to_lines([&](int r) { return a.e.x + (size_t)r * a.e.K; }, a.norm_w, a.eps, R, a.e.K, xn_u, red_norm,
+                           bar);
     int stage = 0;
     uint32_t phase = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {

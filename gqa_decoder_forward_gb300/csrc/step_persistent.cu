@@ -1,0 +1,497 @@
+// One decode step of one or two rows as a single persistent launch: the
+// embedding, every decoder layer and the final norm + lm_head (the decode
+// loop of pull request #1415, section "How", without a launch per operation).
+//
+// One CTA per SM (cooperative launch, so every CTA is resident), 288 threads:
+// warp 8 is a TMA producer, warps 0..7 consume.  The step is a fixed sequence
+// of phases separated by grid barriers:
+//   per layer: RMSNorm + QKV + RoPE + KV append | attention block partials |
+//              merge | o + residual | RMSNorm + gate/up + SwiGLU | down + residual
+//   then: final RMSNorm + lm_head.
+// The producer walks the same sequence as the consumers and keeps a ring of
+// eight 16 KB shared-memory stages full: the weight stages of the projections
+// and the key/value tiles of the attention units (128 positions x 64 dims per
+// stage, four stages per unit) stream in while the consumers are still at a
+// barrier, so each phase starts with data in place instead of paying a
+// launch, a pipeline fill and a tail.  Only the key/value block holding this
+// step's own rows waits for the barrier after the QKV phase.
+//
+// Every phase runs the arithmetic of the separate decode kernels (the shared
+// device code of matvec_core.cuh and attn_core.cuh, the same work units and
+// the same reduction orders), so a row's results are bit-identical to those
+// of the multi-launch path: one-row steps here equal windows there.
+//
+// Grid barrier: thread 0 of each CTA fences, adds one to a counter and waits
+// (acquire loads, bounded) until it reaches (barrier index) x (CTAs).  Every
+// wait in the kernel is bounded; a timeout sets the device status and an abort
+// flag that ends every other wait, and the kernel returns.
+#include <cuda.h>
+
+#include "attn_core.cuh"
+#include "common.cuh"
+#include "matvec_core.cuh"
+#include "tma.cuh"
+
+namespace tfl {
+namespace {
+
+using mvc::kABytes;
+using mvc::kConsumerWarps;
+using mvc::kKbPerStage;
+
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kDepth = 8;
+constexpr int kStage = kABytes;                       // 16 KB: one weight stage or one K/V tile
+constexpr int kXsBytes = kStepMaxRows * 22016 * 2;    // activation lines / attention / merge scratch
+constexpr int kRedBytes = kConsumerWarps * 4 * 32 * 4;
+constexpr int kPhasesPerLayer = 6;
+constexpr uint32_t kSpinLimit = 1u << 24;
+
+enum Phase { PH_QKV, PH_ATTN, PH_MERGE, PH_O, PH_GATEUP, PH_DOWN, PH_HEAD };
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// The projection of a matvec phase, as the separate kernels describe it.
+__device__ __forceinline__ MatvecArgs phase_args(const StepArgs& a, int l, int ph) {
+    MatvecArgs e = {};
+    e.n_rows = a.rows.n_rows;
+    switch (ph) {
+        case PH_QKV:
+            e.mode = MV_QKV_ROPE;
+            e.K = a.H;
+            e.n_q = a.n_q;
+            e.n_kv = a.n_kv;
+            e.y = a.q;
+            e.ldy = a.n_q * kHeadDim;
+            e.cos_t = a.cos_t;
+            e.sin_t = a.sin_t;
+            e.layer = l;
+            e.rows = a.rows;
+            break;
+        case PH_O:
+            e.mode = MV_RESIDUAL;
+            e.K = a.n_q * kHeadDim;
+            e.n_out = a.H;
+            e.h = a.h;
+            break;
+        case PH_GATEUP:
+            e.mode = MV_SWIGLU;
+            e.K = a.H;
+            e.n_out = a.F;
+            e.y = a.act;
+            e.ldy = a.F;
+            break;
+        case PH_DOWN:
+            e.mode = MV_RESIDUAL;
+            e.K = a.F;
+            e.n_out = a.H;
+            e.h = a.h;
+            break;
+        default:  // PH_HEAD
+            e.mode = MV_STORE;
+            e.K = a.H;
+            e.n_out = a.V;
+            e.y = a.logits;
+            e.ldy = a.V;
+            break;
+    }
+    return e;
+}
+
+__device__ __forceinline__ const CUtensorMap* phase_maps(const StepArgs& a, int l, int ph) {
+    switch (ph) {
+        case PH_QKV: return a.wmaps + l * 7 + 0;
+        case PH_O: return a.wmaps + l * 7 + 3;
+        case PH_GATEUP: return a.wmaps + l * 7 + 4;
+        case PH_DOWN: return a.wmaps + l * 7 + 6;
+        default: return a.wmaps + a.layers * 7;
+    }
+}
+
+__device__ __forceinline__ int phase_tiles(const MatvecArgs& e) {
+    if (e.mode == MV_SWIGLU) return e.n_out / 8;
+    if (e.mode == MV_QKV_ROPE) return (e.n_q + 2 * e.n_kv) * 8;
+    return e.n_out / 16;
+}
+
+// Attention unit u of the step (the decode kernels' grid: key block, KV head,
+// group of up to four rows of one stream); false when the block lies past
+// every row of its group.  late: the block holds positions written this step.
+struct Unit {
+    int s, b, g, r0, nr, p_first, k0, nv;
+    bool late;
+};
+__device__ __forceinline__ bool attn_unit(const StepArgs& a, int u, int nblk, Unit& x) {
+    x.b = u % nblk;
+    const int rest = u / nblk;
+    x.g = rest % a.n_kv;
+    int z = rest / a.n_kv;
+    bool found = false;
+    for (int t = 0; t < a.rows.n_streams && !found; ++t) {
+        const int rows = a.rows.row_start[t + 1] - a.rows.row_start[t];
+        const int ng = (rows + 3) / 4;
+        if (z < ng) {
+            x.s = t;
+            x.r0 = a.rows.row_start[t] + z * 4;
+            x.nr = min(4, rows - z * 4);
+            found = true;
+        } else {
+            z -= ng;
+        }
+    }
+    if (!found) return false;
+    x.p_first = a.rows.pos0[x.s] + (x.r0 - a.rows.row_start[x.s]);
+    const int p_last = x.p_first + x.nr - 1;
+    x.k0 = x.b * kPage;
+    if (x.k0 > p_last) return false;
+    x.nv = min(kPage, p_last + 1 - x.k0);
+    x.late = x.k0 + x.nv > a.rows.pos0[x.s];
+    return true;
+}
+
+__device__ __forceinline__ int attn_blocks(const StepArgs& a) {
+    int max_pos = 0;
+    for (int s = 0; s < a.rows.n_streams; ++s)
+        max_pos = max(max_pos, a.rows.pos0[s] + a.rows.row_start[s + 1] - a.rows.row_start[s] - 1);
+    return max_pos / kPage + 1;
+}
+
+__device__ __forceinline__ int attn_groups(const StepArgs& a) {
+    int g = 0;
+    for (int s = 0; s < a.rows.n_streams; ++s) g += (a.rows.row_start[s + 1] - a.rows.row_start[s] + 3) / 4;
+    return g;
+}
+
+// Waits until the grid barrier counter reaches target; false on timeout or abort.
+__device__ __forceinline__ bool wait_counter(const StepArgs& a, unsigned target) {
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        if (ld_acquire(a.sync) >= target) return true;
+        if (*((volatile unsigned*)a.sync + 1) != 0u) return false;
+        if (i >= 32) __nanosleep(64);
+    }
+    atomicOr(a.status, kStatusDevice);
+    atomicExch(a.sync + 1, 1u);
+    return false;
+}
+
+struct ConsumerBar {
+    __device__ __forceinline__ void operator()() const { named_barrier(1, kConsumerWarps * 32); }
+};
+
+struct RingPos {
+    int stage;
+    uint32_t phase;
+    __device__ __forceinline__ void advance() {
+        if (++stage == kDepth) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// ---- producer (warp 8, lane 0) ------------------------------------------------
+// Fills the ring in exactly the order the consumers drain it.
+__device__ void producer(const StepArgs& a, unsigned char* ring, uint64_t* full, uint64_t* empty,
+                         volatile int* s_abort) {
+    const uint64_t pol = policy_evict_first();
+    const int G = gridDim.x;
+    const int nblk = attn_blocks(a), units = nblk * a.n_kv * attn_groups(a);
+    RingPos rp{0, 0u};
+    auto take = [&]() -> unsigned char* {
+        if (*s_abort || !mbar_wait(&empty[rp.stage], rp.phase ^ 1u, a.status)) {
+            *s_abort = 1;
+            return nullptr;
+        }
+        mbar_arrive_expect_tx(&full[rp.stage], kStage);
+        return ring + rp.stage * kStage;
+    };
+    auto weights = [&](int l, int ph) -> bool {
+        const MatvecArgs e = phase_args(a, l, ph);
+        const CUtensorMap* maps = phase_maps(a, l, ph);
+        const int tiles = phase_tiles(e), nst = (e.K + 511) / 512;
+        for (int t = blockIdx.x; t < tiles; t += G)
+            for (int ks = 0; ks < nst; ++ks) {
+                unsigned char* sA = take();
+                if (!sA) return false;
+                mvc::load_weights(e, maps, t, ks * kKbPerStage, sA, &full[rp.stage], pol);
+                rp.advance();
+            }
+        return true;
+    };
+    for (int l = 0; l < a.layers; ++l) {
+        if (!weights(l, PH_QKV)) return;
+        // key/value tiles: blocks written by earlier steps first; the block(s)
+        // holding this step's rows once every CTA has passed the QKV phase
+        bool waited = false;
+        for (int pass = 0; pass < 2; ++pass)
+            for (int u = blockIdx.x; u < units; u += G) {
+                Unit x;
+                if (!attn_unit(a, u, nblk, x) || (int)x.late != pass) continue;
+                if (x.late && !waited) {
+                    if (!wait_counter(a, (unsigned)(l * kPhasesPerLayer + 1) * (unsigned)G)) {
+                        *s_abort = 1;
+                        return;
+                    }
+                    // the rows were written by generic stores of other CTAs; TMA reads through the async proxy
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    waited = true;
+                }
+                const KvView& kv = a.rows.kv[x.s];
+                const int page = __ldg(kv.table + x.b);
+                for (int part = 0; part < 4; ++part) {  // K dims 0-63, K 64-127, V 0-63, V 64-127
+                    unsigned char* dst = take();
+                    if (!dst) return;
+                    const int row0 = ((l * 2 + (part >> 1)) * kv.n_pages + page) * kPage;
+                    tma_load_3d(dst, &a.kvmap[x.s], (part & 1) * 64, x.g, row0, &full[rp.stage], pol);
+                    rp.advance();
+                }
+            }
+        if (!weights(l, PH_O) || !weights(l, PH_GATEUP) || !weights(l, PH_DOWN)) return;
+    }
+    weights(0, PH_HEAD);
+}
+
+// ---- consumers (warps 0..7) ------------------------------------------------------
+template <int GQ>
+__device__ __forceinline__ void attention_unit(const StepArgs& a, const AttnDecodeArgs& at, const Unit& x,
+                                               unsigned char* ring, unsigned char* xs, uint64_t* full, RingPos rp,
+                                               volatile int* s_abort) {
+    const int tid = threadIdx.x;
+    const ConsumerBar bar;
+    const int P = x.nr * GQ, MT = (P + 15) / 16;
+    const uint32_t xs_u = smem_u32(xs);
+    const uint32_t q_u = xs_u, p_u = xs_u + attn::kMaxPairs * kHeadDim * 2;
+    float(*wmax)[attn::kMaxPairs] = reinterpret_cast<float(*)[attn::kMaxPairs]>(xs + 3 * attn::kMaxPairs * kHeadDim * 2);
+    float(*wsum)[attn::kMaxPairs] = wmax + attn::kWarps;
+    // queries of the group's (row, head) pairs; pairs past P are zero
+    for (int i = tid; i < MT * 16 * 16; i += kConsumerWarps * 32) {
+        const int p = i >> 4, c = i & 15;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (p < P) {
+            const int row = x.r0 + p / GQ, head = x.g * GQ + p % GQ;
+            val = *reinterpret_cast<const uint4*>(a.q + (size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + c * 8);
+        }
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(q_u + 2u * attn::swz(p, c * 8)), "r"(val.x),
+                     "r"(val.y), "r"(val.z), "r"(val.w)
+                     : "memory");
+    }
+    RingPos s[4];
+    s[0] = rp;
+    for (int j = 1; j < 4; ++j) {
+        s[j] = s[j - 1];
+        s[j].advance();
+    }
+    for (int j = 0; j < 2; ++j)
+        if (!*s_abort && !mbar_wait(&full[s[j].stage], s[j].phase, a.status)) *s_abort = 1;
+    bar();
+    // stage tiles written by TMA with 128-byte swizzle: row r (a position), 64 dims
+    const uint32_t k0u = smem_u32(ring + s[0].stage * kStage), k1u = smem_u32(ring + s[1].stage * kStage);
+    const uint32_t v0u = smem_u32(ring + s[2].stage * kStage), v1u = smem_u32(ring + s[3].stage * kStage);
+    auto tile_addr = [](uint32_t lo, uint32_t hi, int row, int col) {
+        return (col < 64 ? lo : hi) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4);
+    };
+    attn::BlockGeom bg;
+    bg.b = x.b;
+    bg.g = x.g;
+    bg.r0 = x.r0;
+    bg.P = P;
+    bg.MT = MT;
+    bg.k0 = x.k0;
+    bg.nv = x.nv;
+    bg.p_first = x.p_first;
+    attn::block_partial<GQ>(
+        at, bg, q_u, p_u, wmax, wsum, [&](int row, int col) { return tile_addr(k0u, k1u, row, col); },
+        [&](int row, int col) { return tile_addr(v0u, v1u, row, col); }, bar,
+        [&] {
+            for (int j = 2; j < 4; ++j)
+                if (!*s_abort && !mbar_wait(&full[s[j].stage], s[j].phase, a.status)) *s_abort = 1;
+            if (x.nv < kPage) {
+                // values past the last visible key must be exact zeros (their weight is 0)
+                const int n16 = (kPage - x.nv) * 8;  // 16-byte chunks per stage
+                for (int i = tid; i < 2 * n16; i += kConsumerWarps * 32) {
+                    const uint32_t base = i < n16 ? v0u : v1u;
+                    const int c = i < n16 ? i : i - n16;
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(base + x.nv * 128 + c * 16), "r"(0u)
+                                 : "memory");
+                }
+                // the stage is refilled by TMA later: order these generic writes before it
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            bar();
+        });
+}
+
+__device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char* xs, float* red, float* red_norm,
+                          uint64_t* full, uint64_t* empty, volatile int* s_abort) {
+    const int tid = threadIdx.x, lane = tid & 31, tig = lane & 3;
+    const int R = a.rows.n_rows, G = gridDim.x;
+    const int QD = a.n_q * kHeadDim, GQ = a.n_q / a.n_kv;
+    const ConsumerBar bar;
+    const uint32_t ring_u = smem_u32(ring), xs_u = smem_u32(xs);
+    RingPos rp{0, 0u};
+    unsigned epoch = 0;
+    const int nblk = attn_blocks(a), units = nblk * a.n_kv * attn_groups(a);
+    AttnDecodeArgs at = {};
+    at.q = a.q;
+    at.out = a.ao;
+    at.pm = a.pm;
+    at.pl = a.pl;
+    at.po = a.po;
+    at.max_blocks = a.max_blocks;
+    at.n_q = a.n_q;
+    at.n_kv = a.n_kv;
+    at.rows = a.rows;
+
+    auto grid_barrier = [&]() -> bool {
+        bar();  // this CTA's writes of the phase are done
+        ++epoch;
+        if (tid == 0) {
+            __threadfence();
+            atomicAdd(a.sync, 1u);
+            if (!wait_counter(a, epoch * (unsigned)G)) *s_abort = 1;
+        }
+        bar();
+        return !*s_abort;
+    };
+    auto matvec = [&](int l, int ph, auto row, const bf16* norm_w) {
+        const MatvecArgs e = phase_args(a, l, ph);
+        const int tiles = phase_tiles(e), nst = (e.K + 511) / 512, kblocks = e.K / 64;
+        mvc::rows_to_lines(row, norm_w, a.eps, R, e.K, xs_u, red_norm, bar);
+        for (int t = blockIdx.x; t < tiles; t += G)
+            mvc::consume_tile<1>(e, t, nst, R, ring_u, kStage, kDepth, rp.stage, rp.phase, full, empty, red, s_abort,
+                                 a.status, mvc::XFromLines{xs_u, R, kblocks, tig}, bar);
+    };
+    auto hrow = [&](int r) { return (const bf16*)a.h + (size_t)r * a.H; };
+    auto aorow = [&](int r) { return (const bf16*)a.ao + (size_t)r * QD; };
+    auto actrow = [&](int r) { return (const bf16*)a.act + (size_t)r * a.F; };
+    auto erow = [&](int r) {
+        const int id = a.ids[r];
+        return (id >= 0 && id < a.V) ? a.embed + (size_t)id * a.H : a.zero_row;
+    };
+
+    for (int l = 0; l < a.layers; ++l) {
+        // RMSNorm + QKV + RoPE + KV append
+        if (l == 0) {
+            // the residual stream starts as the embedding rows (zeros for an id out of range)
+            if (blockIdx.x == 0) {
+                for (int r = 0; r < R; ++r)
+                    for (int i = tid * 8; i < a.H; i += kConsumerWarps * 32 * 8)
+                        *reinterpret_cast<uint4*>(a.h + (size_t)r * a.H + i) =
+                            *reinterpret_cast<const uint4*>(erow(r) + i);
+                if (tid == 0)
+                    for (int r = 0; r < R; ++r)
+                        if (a.ids[r] < 0 || a.ids[r] >= a.V) atomicOr(a.status, kStatusBadToken);
+            }
+            matvec(0, PH_QKV, erow, a.norms[0]);
+        } else {
+            matvec(l, PH_QKV, hrow, a.norms[2 * l]);
+        }
+        if (!grid_barrier()) return;
+        // attention block partials: blocks written by earlier steps, then this step's
+        at.layer = l;
+        for (int pass = 0; pass < 2; ++pass)
+            for (int u = blockIdx.x; u < units; u += G) {
+                Unit x;
+                if (!attn_unit(a, u, nblk, x) || (int)x.late != pass) continue;
+                bar();  // the previous unit is done with the queries and weights
+                if (GQ == 7)
+                    attention_unit<7>(a, at, x, ring, xs, full, rp, s_abort);
+                else
+                    attention_unit<8>(a, at, x, ring, xs, full, rp, s_abort);
+                __syncwarp();
+                if (lane == 0)
+                    for (int j = 0; j < 4; ++j) {
+                        mbar_arrive(&empty[rp.stage]);
+                        rp.advance();
+                    }
+                else
+                    for (int j = 0; j < 4; ++j) rp.advance();
+            }
+        if (!grid_barrier()) return;
+        // merge: one (row, head) per unit
+        {
+            float* wts = reinterpret_cast<float*>(xs);
+            float* redm = wts + 1024;
+            float(*so)[kHeadDim] = reinterpret_cast<float(*)[kHeadDim]>(wts + 1024 + 16);
+            float* sl = wts + 1024 + 16 + attn::kMergeSlices * kHeadDim;
+            for (int u = blockIdx.x; u < R * a.n_q; u += G) {
+                bar();
+                attn::merge<kConsumerWarps * 32>(at, u / a.n_q, u % a.n_q, tid, wts, redm, so, sl, bar);
+            }
+        }
+        if (!grid_barrier()) return;
+        matvec(l, PH_O, aorow, nullptr);
+        if (!grid_barrier()) return;
+        matvec(l, PH_GATEUP, hrow, a.norms[2 * l + 1]);
+        if (!grid_barrier()) return;
+        matvec(l, PH_DOWN, actrow, nullptr);
+        if (!grid_barrier()) return;
+    }
+    matvec(0, PH_HEAD, hrow, a.final_norm);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* ring =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* xs = ring + kDepth * kStage;
+    float* red = reinterpret_cast<float*>(xs + kXsBytes);
+    float* red_norm = red + kRedBytes / 4;
+    uint64_t* full = reinterpret_cast<uint64_t*>(red_norm + 8 * kStepMaxRows);
+    uint64_t* empty = full + kDepth;
+    volatile int* s_abort = reinterpret_cast<volatile int*>(empty + kDepth);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kDepth; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        *s_abort = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            producer(a, ring, full, empty, s_abort);
+            // after an abort, give copies already issued time to land before the CTA ends
+            if (*s_abort) __nanosleep(500000);
+        }
+        return;
+    }
+    consumers(a, ring, xs, red, red_norm, full, empty, s_abort);
+}
+
+}  // namespace
+
+int step_smem_bytes() {
+    return 1024 + kDepth * kStage + kXsBytes + kRedBytes + 8 * kStepMaxRows * 4 + 2 * kDepth * 8 + 64;
+}
+
+cudaError_t init_step_persistent() {
+    return cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, step_smem_bytes());
+}
+
+cudaError_t launch_step_persistent(const StepArgs& a, int grid, cudaStream_t st) {
+    if (a.rows.n_rows < 1 || a.rows.n_rows > kStepMaxRows || a.rows.n_streams > kStepMaxRows || a.n_kv < 1 ||
+        (a.n_q / a.n_kv != 7 && a.n_q / a.n_kv != 8) || a.n_q % a.n_kv != 0 || a.F > 22016)
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaMemsetAsync(a.sync, 0, 2 * sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = step_smem_bytes();
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, step_kernel, a);
+}
+
+}  // namespace tfl

@@ -77,6 +77,7 @@ SIGNATURES = {
                                     _vp]),
     "tfl_attention_decode_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp]),
     "tfl_profile": (ctypes.c_int, [_vp, ctypes.c_int]),
+    "tfl_set_persistent": (ctypes.c_int, [_vp, ctypes.c_int]),
     "tfl_profile_read": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_long)]),
     "tfl_profile_kind": (ctypes.c_char_p, [ctypes.c_int]),
@@ -194,6 +195,11 @@ class Model:
     def decode_step(self, kvs: Sequence["KV"], ids: torch.Tensor, rows: Sequence[int], logits: torch.Tensor,
                     stream=None):
         return tfl_decode_step(self, kvs, ids, rows, logits, stream)
+
+    def set_persistent(self, enable: bool):
+        """Decode steps of one or two rows as one persistent launch (default) or
+        as a launch per operation; the results are bit-identical."""
+        return _check(lib().tfl_set_persistent(self.handle, 1 if enable else 0))
 
     def prefill_chunk(self, kv: "KV", ids: torch.Tensor, logits=None, all_rows=False, stream=None):
         return tfl_prefill_chunk(self, kv, ids, logits, all_rows, stream)

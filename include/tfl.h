@@ -194,6 +194,17 @@ int tfl_decode_step(tfl_model* model, tfl_kv* const* kvs, int n_streams, const i
                     const int* rows_per_stream, void* logits, void* stream);
 
 /*
+ * A decode step of one or two rows in total runs, by default, as one
+ * persistent cooperative launch (all layers and the head; one CTA per SM, grid
+ * barriers between the operations) with the same arithmetic as the launch per
+ * operation used for larger steps, so results are bit-identical either way.
+ * enable = 0 makes every step use the launch per operation (for comparisons);
+ * enable != 0 restores the default.  No counterpart on the pages (an execution
+ * detail of this library).
+ */
+int tfl_set_persistent(tfl_model* model, int enable);
+
+/*
  * Prompt chunk of n_rows (1..max_rows) ids (device int32) for one stream, at
  * positions length .. length + n_rows - 1 (causal over the cache and the
  * chunk).  logits: NULL for none; else device bf16 [1][V] for the last row
