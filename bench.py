@@ -289,7 +289,7 @@ def run_tfl(args, world, rank, local):
     tfl.lib()
     shape = SHAPE.with_layers(args.layers)
     ctx = args.context
-    extra = args.warmup + args.steps + 16 + 16 + 8
+    extra = args.warmup + args.steps + 16 + 16 + 18 + 8  # warm-up, timed, profiled, e2e, per-launch steps
     max_ctx = ctx + extra
     dev = torch.device("cuda", torch.cuda.current_device())
 
@@ -362,6 +362,20 @@ def run_tfl(args, world, rank, local):
     tfl.tfl_profile(model, False)
     launches_per_step = sum(n for _, n in prof.values()) / prof_steps
 
+    # the same steps with a launch per operation (the path larger steps take)
+    model.set_persistent(False)
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(st)
+    for _ in range(prof_steps):
+        step()
+    a1.record(st)
+    torch.cuda.synchronize()
+    per_launch_ms = a0.elapsed_time(a1) / prof_steps
+    model.set_persistent(True)
+
     # end to end through the C ABI with host buffers: id in (pinned, H2D), id out (D2H)
     e2e_steps = min(16, args.steps)
     host_in = torch.empty(1, dtype=torch.int32, pin_memory=True)
@@ -392,6 +406,8 @@ def run_tfl(args, world, rank, local):
         "matvec_qkv_rope": (shape.n_q + 2 * shape.n_kv) * 128 * H * 2 + H * 2,
         "matvec_o_residual": H * H * 2 + 3 * H * 2,
         "matvec_lm_head": shape.vocab * H * 2 + H * 2 + shape.vocab * 2,
+        # the whole step in one launch: every weight byte and the visible KV
+        "decode_step_persistent": step_b,
     }.get(dom_name)
     roof = None
     if dom_bytes is not None:
@@ -426,6 +442,7 @@ def run_tfl(args, world, rank, local):
         "kv": args.kv,
         "kernels": {k: {"ms_per_step": round(v[0] / prof_steps, 4), "launches_per_step": v[1] / prof_steps}
                     for k, v in prof.items() if v[1]},
+        "per_launch_path_ms_per_step": round(per_launch_ms, 4),
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "e2e": {"value": round(world / e2e_s, 3), "unit": "tok/s", "h2d_bytes_per_step": 4,
                 "d2h_bytes_per_step": 4},

@@ -99,7 +99,7 @@ Layout layout(const tfl_config* c) {
     Layout L;
     const size_t rows = (size_t)std::max(c->max_rows, c->max_decode_rows);
     const size_t dr = (size_t)c->max_decode_rows;
-    L.max_blocks = (c->max_context + kPage - 1) / kPage;
+    L.max_blocks = (c->max_context + kAttnUnit - 1) / kAttnUnit;  // decode-attention units per row
     const size_t qd = (size_t)c->n_q * kHeadDim;
     size_t off = 0;
     auto take = [&](size_t bytes) {

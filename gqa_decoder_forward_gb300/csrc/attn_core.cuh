@@ -1,15 +1,14 @@
 // The arithmetic of decode attention, shared by the split attention kernels and
 // the persistent decode-step kernel so that both give the same bits.
 //
-// Block partial (one 128-key block at absolute positions, one KV head, a group
-// of rows): eight warps; S = Q K^T with warp w owning keys 16w..16w+15, scale
-// by log2(e)/sqrt(128) and causal mask, block row max over the warps, weights
-// p = 2^(s - max) split into hi/lo bf16, row sums, then O = P V with warp w
-// owning dims 16w..16w+15.  Written per (row, head): m_b, l_b and o_b.
-// Merge: per (row, head), M = max_b m_b, then L = sum l_b 2^(m_b - M) and
-// O = sum o_b 2^(m_b - M), each folded over eight block slices (slice i takes
-// blocks i, i+8, ...) in block order and the slices added in slice order;
-// out = bf16(O / L).
+// Unit partial (512 keys at absolute positions, one KV head, a group of up to
+// two rows): warp w of eight owns keys 16w..16w+15 of each 128-key sub-block
+// and runs an online softmax over them (S = Q K^T scaled by log2(e)/sqrt(128)
+// and causally masked, running max, weights p = 2^(s - max) split into hi/lo
+// bf16, running sums, O = P V); the warp partials are then combined in warp
+// order.  Written per (row, head): m_u, l_u and o_u.
+// Merge: per (row, head), M = max_u m_u, then L = sum l_u 2^(m_u - M) and
+// O = sum o_u 2^(m_u - M) folded in unit order; out = bf16(O / L).
 #pragma once
 
 #include "common.cuh"
@@ -20,8 +19,6 @@ namespace attn {
 
 constexpr int kWarps = 8;            // warps taking part (256 threads)
 constexpr int kKB = kPage;           // keys per block
-constexpr int kMaxPairs = 32;        // up to 4 rows x 8 heads: two m16 tiles
-constexpr int kMergeSlices = 8;
 constexpr float kScale = 0.12751743074640502f;  // log2(e) / sqrt(128)
 
 // Rows of 128 bf16 (256 bytes, 16 chunks of 16 bytes) with chunk c of row r
@@ -31,247 +28,263 @@ __device__ __forceinline__ int swz(int row, int col) {
     return row * kHeadDim + (((col >> 3) ^ (row & 7)) << 3) + (col & 7);
 }
 
-struct BlockGeom {
-    int b, g;        // key block, KV head
-    int r0, P, MT;   // first row of the group (call-wide index), pairs, m16 tiles of pairs
-    int k0, nv;      // first key, keys of the block any row of the group sees
-    int p_first;     // position of the group's first row
+// A unit is 512 keys at absolute positions (kUnit): up to four sub-blocks of
+// 128 keys (one cache page each).  Warp w of the eight owns keys 16w..16w+15 of
+// every sub-block and keeps its own running max, sum and output for the
+// unit; the eight warp partials are combined once at the end, in warp order.
+constexpr int kSub = kPage;          // keys per sub-block
+constexpr int kUnit = kAttnUnit;     // keys per unit (one partial per (row, head, unit))
+constexpr int kGroupRows = 2;        // rows per group: G * 2 <= 16 (row, head) pairs, one m16 tile
+constexpr int kPairs = 16;
+constexpr int kCombFloats = kWarps * kPairs * kHeadDim + 2 * kWarps * kPairs;  // combine scratch
+
+struct UnitGeom {
+    int u, g;        // unit, KV head
+    int r0, P;       // first row of the group (call-wide index), (row, head) pairs (<= 16)
+    int k0;          // first key of the unit
+    int nsub;        // sub-blocks holding keys any row of the group sees (1..4)
+    int p_first, p_last;  // positions of the group's first and last rows
 };
 
-// One block partial.  q_u: shared address of the queries (kMaxPairs x 128 bf16,
-// swz layout; pairs past P zero).  p_u: shared address for the weights (two
-// kMaxPairs x 128 tiles, hi then lo, swz layout); it may alias the keys.
-// kaddr(row, col) / vaddr(row, col): shared address of the 16-byte chunk of key
-// (or value) row `row` holding dims col..col+7.  bar(): barrier of the eight
-// warps.  values_ready(): makes the values visible (called after the weights
-// are written, before P V).  wmax/wsum: kWarps x kMaxPairs floats each.
-template <int G, class KA, class VA, class Bar, class VReady>
-__device__ __forceinline__ void block_partial(const AttnDecodeArgs& a, const BlockGeom& bg, uint32_t q_u, uint32_t p_u,
-                                              float (*wmax)[kMaxPairs], float (*wsum)[kMaxPairs], KA kaddr, VA vaddr,
-                                              Bar bar, VReady values_ready) {
+// One unit partial by the eight warps (threads 0..255).  q_u: shared address
+// of the queries (16 pairs x 128 bf16, swz layout, pairs past P zero), visible
+// to every warp.  comb: kCombFloats floats of shared memory.  src provides,
+// for sub-block j: wait(j) (this warp may read the sub-block's keys and
+// values; values past the last visible key are exact zeros), done(j) (this
+// warp has read its last key and value of j), k(j, row, col) / v(j, row, col)
+// (shared address of the 16-byte chunk of key / value row `row` holding dims
+// col..col+7).  bar(): barrier of the eight warps.
+//
+// The products are taken transposed so that keys (and dims) fill the 16-row
+// side of the m16n8k16 tensor-core shape and the (row, head) pairs the 8-wide
+// side: S^T = K Q^T, then O^T += V^T P^T with P^T moved from the accumulator
+// layout into the operand layout by an in-register transpose (movmatrix).
+// Warp w, per pair and sub-block j, over its 16 keys: scores
+// s = (q . k) log2(e)/sqrt(128) (masked: -inf), m_new = max(m, max s),
+// alpha = 2^(m - m_new), p = 2^(s - m_new), l = l alpha + sum p (the thread's
+// two keys in order, then a fixed shuffle tree over the warp's keys),
+// O = O alpha + P V (hi part, then lo part).  Combine: M = max_w m_w,
+// a_w = 2^(m_w - M), L = sum_w l_w a_w, O = sum_w O_w a_w (fused multiply-adds
+// in warp order).  A pair with no visible key keeps m = -inf, l = 0, O = 0.
+template <int G, int NP, class Src, class Bar>
+__device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const UnitGeom& ug, uint32_t q_u,
+                                                float* comb, Src& src, Bar bar) {
     using wm::ldsm_x4;
     using wm::ldsm_x4_t;
     using wm::mma16816;
+    using wm::movmatrix_t;
     using wm::pack_bf16;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;  // threads 0..255
     const int gq = lane >> 2, tig = lane & 3;
-    const int P = bg.P, MT = bg.MT, nv = bg.nv, k0 = bg.k0;
+    const int P = ug.P;  // NP = (P + 7) / 8 n8 tiles of pairs
+    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;  // A (non-trans): 16 x 16
+    const int trow = (lane & 7) + (lane >> 4) * 8, tcol = ((lane >> 3) & 1) * 8;  // A (trans): 16 x 16
 
-    // ---- S = Q K^T: warp w owns keys 16w .. 16w+15 (two n8 tiles) ----
-    float sc[2][2][4];  // [m tile][n tile][fragment]
+    // Q^T as B fragments: [n tile][k step][2]
+    uint32_t qb[NP][kHeadDim / 16][2];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int nt = 0; nt < NP; ++nt) {
+        {
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.f;
-    {
-        const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8, mcol = (lane >> 4) * 8;  // A: matrices (r, k) quads
-        const int krow = (lane & 7) + (lane >> 4) * 8, kcol = ((lane >> 3) & 1) * 8;  // B: keys x dims
+            for (int ks = 0; ks < kHeadDim / 16; ks += 2) {
+                uint32_t r[4];
+                ldsm_x4(r, q_u + 2u * swz(nt * 8 + (lane & 7), ks * 16 + (lane >> 3) * 8));
+                qb[nt][ks][0] = r[0];
+                qb[nt][ks][1] = r[1];
+                qb[nt][ks + 1][0] = r[2];
+                qb[nt][ks + 1][1] = r[3];
+            }
+        }
+    }
+    // this thread's pairs: nt * 8 + 2 * tig + e
+    int pos_p[NP][2];
+#pragma unroll
+    for (int nt = 0; nt < NP; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int p = nt * 8 + 2 * tig + e;
+            pos_p[nt][e] = p < P ? ug.p_first + p / G : -1;  // -1: a padding pair sees nothing
+        }
+    float m_w[NP][2], l_w[NP][2];
+    float ot[kHeadDim / 16][NP][4];  // [dim tile][pair tile][fragment]
+#pragma unroll
+    for (int nt = 0; nt < NP; ++nt) {
+        m_w[nt][0] = m_w[nt][1] = -INFINITY;
+        l_w[nt][0] = l_w[nt][1] = 0.f;
+#pragma unroll
+        for (int dt = 0; dt < kHeadDim / 16; ++dt) ot[dt][nt][0] = ot[dt][nt][1] = ot[dt][nt][2] = ot[dt][nt][3] = 0.f;
+    }
+
+    for (int j = 0; j < ug.nsub; ++j) {
+        const int kj = ug.k0 + j * kSub;
+        const int nv = min(kSub, ug.p_last + 1 - kj);  // keys of the sub-block any row sees
+        src.wait(j);
+        // ---- S^T = K Q^T: 16 keys (rows gq, gq+8) x 8 pairs per tile ----
+        float st[NP][4];
+#pragma unroll
+        for (int nt = 0; nt < NP; ++nt) st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-            uint32_t bk[4];
-            ldsm_x4(bk, kaddr(warp * 16 + krow, ks * 16 + kcol));
+            uint32_t ak[4];
+            ldsm_x4(ak, src.k(j, warp * 16 + arow, ks * 16 + acol));
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                if (mt < MT) {
-                    uint32_t aq[4];
-                    ldsm_x4(aq, q_u + 2u * swz(mt * 16 + mrow, ks * 16 + mcol));
-                    mma16816(sc[mt][0], aq, bk[0], bk[1]);
-                    mma16816(sc[mt][1], aq, bk[2], bk[3]);
+            for (int nt = 0; nt < NP; ++nt)
+                mma16816(st[nt], ak, qb[nt][ks][0], qb[nt][ks][1]);
+        }
+        // ---- per pair: running max, weights, running sums; P^T operands ----
+        uint32_t pbh[NP][2], pbl[NP][2];  // [pair tile][keys 0-7 / 8-15]
+#pragma unroll
+        for (int nt = 0; nt < NP; ++nt) {
+            float alpha[2], pe[2][2];  // pe[key half][pair e]
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int hk = 0; hk < 2; ++hk) {
+                    const int t = warp * 16 + gq + hk * 8;
+                    const bool vis = t < nv && kj + t <= pos_p[nt][e];
+                    float& v = st[nt][hk * 2 + e];
+                    v = vis ? v * kScale : -INFINITY;
+                    mx = fmaxf(mx, v);
                 }
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_new = fmaxf(m_w[nt][e], mx);
+                const bool none = m_new == -INFINITY;
+                alpha[e] = none ? 1.f : exp2f(m_w[nt][e] - m_new);
+                m_w[nt][e] = m_new;
+                float l = 0.f;
+#pragma unroll
+                for (int hk = 0; hk < 2; ++hk) {
+                    pe[hk][e] = none ? 0.f : exp2f(st[nt][hk * 2 + e] - m_new);
+                    l += pe[hk][e];
+                }
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                l_w[nt][e] = l_w[nt][e] * alpha[e] + l;
+            }
+#pragma unroll
+            for (int hk = 0; hk < 2; ++hk) {
+                const bf16 h0 = rn(pe[hk][0]), h1 = rn(pe[hk][1]);
+                pbh[nt][hk] = movmatrix_t(pack_bf16(h0, h1));
+                pbl[nt][hk] = movmatrix_t(pack_bf16(rn(pe[hk][0] - bf(h0)), rn(pe[hk][1] - bf(h1))));
+            }
+#pragma unroll
+            for (int dt = 0; dt < kHeadDim / 16; ++dt) {
+                ot[dt][nt][0] *= alpha[0];
+                ot[dt][nt][1] *= alpha[1];
+                ot[dt][nt][2] *= alpha[0];
+                ot[dt][nt][3] *= alpha[1];
             }
         }
-    }
-    // scale, mask, per-warp row maxima
-    float mx[2][2];  // [m tile][row half]
+        // ---- O^T += V^T P^T over this warp's 16 keys: 8 dim tiles ----
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+        for (int dt = 0; dt < kHeadDim / 16; ++dt) {
+            uint32_t av[4];
+            ldsm_x4_t(av, src.v(j, warp * 16 + trow, dt * 16 + tcol));
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int p = mt * 16 + gq + h * 8;
-            const int pos_row = bg.p_first + (p < P ? p / G : 0);
-            float m = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int t = warp * 16 + nt * 8 + 2 * tig + e;
-                    const bool vis = p < P && t < nv && k0 + t <= pos_row;
-                    float& v = sc[mt][nt][h * 2 + e];
-                    v = vis ? v * kScale : -INFINITY;
-                    m = fmaxf(m, v);
-                }
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            mx[mt][h] = m;
+            for (int nt = 0; nt < NP; ++nt) {
+                mma16816(ot[dt][nt], av, pbh[nt][0], pbh[nt][1]);
+                mma16816(ot[dt][nt], av, pbl[nt][0], pbl[nt][1]);
+            }
         }
+        src.done(j);
     }
-    if (tig == 0) {
+
+    // ---- combine the eight warp partials (warp order) ----
+    float* co = comb;                                   // [warp][pair][dim]
+    float* cm = comb + kWarps * kPairs * kHeadDim;      // [warp][pair]
+    float* cl = cm + kWarps * kPairs;
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+    for (int nt = 0; nt < NP; ++nt) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) wmax[warp][mt * 16 + gq + h * 8] = mx[mt][h];
+        for (int dt = 0; dt < kHeadDim / 16; ++dt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int p = nt * 8 + 2 * tig + e;
+                co[((size_t)warp * kPairs + p) * kHeadDim + dt * 16 + gq] = ot[dt][nt][e];
+                co[((size_t)warp * kPairs + p) * kHeadDim + dt * 16 + gq + 8] = ot[dt][nt][2 + e];
+            }
+        if (gq == 0) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                cm[warp * kPairs + nt * 8 + 2 * tig + e] = m_w[nt][e];
+                cl[warp * kPairs + nt * 8 + 2 * tig + e] = l_w[nt][e];
+            }
+        }
     }
     bar();
-    // block row maxima, weights, per-warp row sums, weights to shared memory
-    float bmax[2][2];
+    const int d = tid & (kHeadDim - 1);
+    for (int p = tid >> 7; p < P; p += 2) {
+        float M = cm[p];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, cm[w * kPairs + p]);
+        float O = 0.f, L = 0.f;
+        if (M != -INFINITY) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int p = mt * 16 + gq + h * 8;
-            float m = wmax[0][p];
-#pragma unroll
-            for (int w = 1; w < kWarps; ++w) m = fmaxf(m, wmax[w][p]);
-            bmax[mt][h] = m;
-            float l = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                float e0 = 0.f, e1 = 0.f;
-                if (m != -INFINITY) {
-                    e0 = exp2f(sc[mt][nt][h * 2 + 0] - m);
-                    e1 = exp2f(sc[mt][nt][h * 2 + 1] - m);
-                }
-                l += e0;
-                l += e1;
-                const bf16 h0 = rn(e0), h1 = rn(e1);
-                const bf16 l0 = rn(e0 - bf(h0)), l1 = rn(e1 - bf(h1));
-                const int t = warp * 16 + nt * 8 + 2 * tig;
-                const uint32_t hi = pack_bf16(h0, h1), lo = pack_bf16(l0, l1);
-                asm volatile("st.shared.u32 [%0], %1;" ::"r"(p_u + 2u * swz(p, t)), "r"(hi) : "memory");
-                asm volatile("st.shared.u32 [%0], %1;" ::"r"(p_u + 2u * (kMaxPairs * kHeadDim + swz(p, t))), "r"(lo)
-                             : "memory");
-            }
-            l += __shfl_xor_sync(0xffffffffu, l, 1);
-            l += __shfl_xor_sync(0xffffffffu, l, 2);
-            if (tig == 0) wsum[warp][p] = l;
-        }
-    }
-    values_ready();
-
-    // ---- O = P V: warp w owns dims 16w .. 16w+15 (two n8 tiles) ----
-    float oc[2][2][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) oc[mt][nt][0] = oc[mt][nt][1] = oc[mt][nt][2] = oc[mt][nt][3] = 0.f;
-    {
-        const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8, mcol = (lane >> 4) * 8;  // A: pairs x keys
-        const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8, vcol = (lane >> 4) * 8;  // B (trans): keys x dims
-#pragma unroll 2
-        for (int ks = 0; ks < kKB / 16; ++ks) {
-            uint32_t bv[4];
-            ldsm_x4_t(bv, vaddr(ks * 16 + vrow, warp * 16 + vcol));
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                if (mt < MT) {
-#pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-                        uint32_t ap[4];
-                        ldsm_x4(ap, p_u + 2u * (part * kMaxPairs * kHeadDim + swz(mt * 16 + mrow, ks * 16 + mcol)));
-                        mma16816(oc[mt][0], ap, bv[0], bv[1]);
-                        mma16816(oc[mt][1], ap, bv[2], bv[3]);
-                    }
-                }
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = cm[w * kPairs + p];
+                const float aw = mw == -INFINITY ? 0.f : exp2f(mw - M);
+                O = fmaf(co[((size_t)w * kPairs + p) * kHeadDim + d], aw, O);
+                L = fmaf(cl[w * kPairs + p], aw, L);
             }
         }
-    }
-
-    // ---- partials: o (unnormalised), m, l per (row, head) ----
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int p = mt * 16 + gq + h * 8;
-            if (mt < MT && p < P) {
-                const int row = bg.r0 + p / G, head = bg.g * G + p % G;
-                const size_t idx = ((size_t)row * a.n_q + head) * a.max_blocks + bg.b;
-                float* po = a.po + idx * kHeadDim + warp * 16 + 2 * tig;
-                *reinterpret_cast<float2*>(po) = make_float2(oc[mt][0][h * 2 + 0], oc[mt][0][h * 2 + 1]);
-                *reinterpret_cast<float2*>(po + 8) = make_float2(oc[mt][1][h * 2 + 0], oc[mt][1][h * 2 + 1]);
-                if (warp == 0 && tig == 0) {
-                    float l = wsum[0][p];
-#pragma unroll
-                    for (int w = 1; w < kWarps; ++w) l += wsum[w][p];
-                    a.pm[idx] = bmax[mt][h];
-                    a.pl[idx] = l;
-                }
-            }
+        const int row = ug.r0 + p / G, head = ug.g * G + p % G;
+        const size_t idx = ((size_t)row * a.n_q + head) * a.max_blocks + ug.u;
+        a.po[idx * kHeadDim + d] = O;
+        if (d == 0) {
+            a.pm[idx] = M;
+            a.pl[idx] = L;
         }
     }
+    bar();  // the combine scratch and the queries may be reused
 }
 
-// Merge of (row, head) by T threads (T = 128 x a divisor of 8): thread tid owns
-// dim tid % 128 and slices tid / 128 + j * (T / 128).  Shared scratch: wts
-// (1,024 floats), red (T / 32 floats), so (8 x 128 floats), sl (8 floats).
-// bar(): barrier of the T threads.
-template <int T, class Bar>
-__device__ __forceinline__ void merge(const AttnDecodeArgs& a, int row, int head, int tid, float* wts, float* red,
-                                      float (*so)[kHeadDim], float* sl, Bar bar) {
-    constexpr int kStep = T / kHeadDim;          // slice step
-    constexpr int kPer = kMergeSlices / kStep;   // slices per thread
-    const int d = tid & (kHeadDim - 1), s0 = tid / kHeadDim;
+template <int G, class Src, class Bar>
+__device__ __forceinline__ void unit_partial(const AttnDecodeArgs& a, const UnitGeom& ug, uint32_t q_u, float* comb,
+                                             Src& src, Bar bar) {
+    if (ug.P <= 8)
+        unit_partial_np<G, 1>(a, ug, q_u, comb, src, bar);
+    else
+        unit_partial_np<G, 2>(a, ug, q_u, comb, src, bar);
+}
+
+// Merge of (row, head) over its units by 128 threads (thread = dim):
+// M = max_u m_u, then O = sum_u o_u 2^(m_u - M) and L = sum_u l_u 2^(m_u - M) as
+// fused multiply-adds in unit order; out = bf16(O / L).  The fold depends
+// only on the row's position (its unit count), never on the other rows.
+__device__ __forceinline__ void merge128(const AttnDecodeArgs& a, int row, int head, int d) {
     const int s = row_stream(a.rows, row);
     const int pos = a.rows.pos0[s] + (row - a.rows.row_start[s]);
-    const int nb = pos / kKB + 1;
+    const int nu = pos / kUnit + 1;
     const size_t base = ((size_t)row * a.n_q + head) * a.max_blocks;
-
     float M = -INFINITY;
-    for (int b = tid; b < nb; b += T) M = fmaxf(M, a.pm[base + b]);
+    for (int u = 0; u < nu; ++u) M = fmaxf(M, a.pm[base + u]);
+    float O = 0.f, L = 0.f;
+    int u = 0;
+    for (; u + 8 <= nu; u += 8) {
+        float mv[8], lv[8], ov[8];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if ((tid & 31) == 0) red[tid >> 5] = M;
-    bar();
-    M = red[0];
+        for (int i = 0; i < 8; ++i) {
+            mv[i] = a.pm[base + u + i];
+            lv[i] = a.pl[base + u + i];
+            ov[i] = a.po[(base + u + i) * kHeadDim + d];
+        }
 #pragma unroll
-    for (int w = 1; w < T / 32; ++w) M = fmaxf(M, red[w]);
-
-    float O[kPer], L[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) O[j] = L[j] = 0.f;
-    for (int c = 0; c < nb; c += 1024) {
-        const int n = min(1024, nb - c);
-        bar();
-        for (int b = tid; b < n; b += T) wts[b] = exp2f(a.pm[base + c + b] - M);
-        bar();
-        const float* pl = a.pl + base + c;
-        const float* po = a.po + (base + c) * kHeadDim + d;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            int b = s0 + j * kStep;
-            for (; b + 7 * kMergeSlices < n; b += 8 * kMergeSlices) {
-                float lv[8], ov[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    lv[u] = pl[b + u * kMergeSlices];
-                    ov[u] = po[(size_t)(b + u * kMergeSlices) * kHeadDim];
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    L[j] = fmaf(lv[u], wts[b + u * kMergeSlices], L[j]);
-                    O[j] = fmaf(ov[u], wts[b + u * kMergeSlices], O[j]);
-                }
-            }
-            for (; b < n; b += kMergeSlices) {
-                L[j] = fmaf(pl[b], wts[b], L[j]);
-                O[j] = fmaf(po[(size_t)b * kHeadDim], wts[b], O[j]);
-            }
+        for (int i = 0; i < 8; ++i) {
+            const float w = exp2f(mv[i] - M);
+            L = fmaf(lv[i], w, L);
+            O = fmaf(ov[i], w, O);
         }
     }
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        so[s0 + j * kStep][d] = O[j];
-        if (d == 0) sl[s0 + j * kStep] = L[j];
+    for (; u < nu; ++u) {
+        const float w = exp2f(a.pm[base + u] - M);
+        L = fmaf(a.pl[base + u], w, L);
+        O = fmaf(a.po[(base + u) * kHeadDim + d], w, O);
     }
-    bar();
-    if (tid < kHeadDim) {
-        float Ot = so[0][d], Lt = sl[0];
-#pragma unroll
-        for (int i = 1; i < kMergeSlices; ++i) {
-            Ot += so[i][d];
-            Lt += sl[i];
-        }
-        a.out[(size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + d] = rn(Ot / Lt);
-    }
+    a.out[(size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + d] = rn(O / L);
 }
 
 }  // namespace attn

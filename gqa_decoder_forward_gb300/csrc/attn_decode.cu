@@ -1,17 +1,19 @@
 // Decode attention: causal GQA of a few rows per stream over a position-major
-// paged bf16 cache, split over key blocks at absolute positions (pull request
+// paged bf16 cache, split over key units at absolute positions (pull request
 // #1415, section "How": "decode rows on sdpa_vector lanes over key blocks at
 // absolute positions").
 //
-// Pass 1 (attn_block_kernel): one CTA per (key block b of 128 positions, KV
-// head g, group of <= 4 rows of one stream).  The block's keys and values for
-// head g are staged in shared memory with cp.async.  The G = n_q/n_kv query
-// heads of the group's rows form the M dimension of tensor-core products
-// (mma.sync m16n8k16, bf16 in, fp32 accumulate): S = Q K^T over the 128 keys,
-// then O = P V.  Per (row, head) the CTA writes the block's max score m_b, sum
-// l_b = sum exp(s - m_b) and o_b = sum exp(s - m_b) v.
-// Pass 2 (attn_merge_kernel): per (row, head), M = max_b m_b, then
-// L = sum_b l_b e^(m_b - M) and O = sum_b o_b e^(m_b - M) in block order,
+// Pass 1 (attn_block_kernel): one CTA per (unit u of 512 positions, KV head g,
+// group of <= 2 rows of one stream).  The unit's four 128-key sub-blocks of
+// head g stream through two shared-memory buffers (cp.async), one computed
+// while the next lands.  The G = n_q/n_kv query heads of the group's rows form
+// the M dimension of tensor-core products (mma.sync m16n8k16, bf16 in, fp32
+// accumulate); warp w owns keys 16w..16w+15 of every sub-block and runs its
+// own online softmax (S = Q K^T, running max, O += P V), the warp partials are
+// combined at the end.  Per (row, head) the CTA writes the unit's max score
+// m_u, sum l_u = sum exp(s - m_u) and o_u = sum exp(s - m_u) v (attn_core.cuh).
+// Pass 2 (attn_merge_kernel): per (row, head), M = max_u m_u, then
+// L = sum_u l_u e^(m_u - M) and O = sum_u o_u e^(m_u - M) in unit order,
 // out = bf16(O / L).
 //
 // Precision: scores are fp32 dot products of the bf16 q and k, scaled in fp32;
@@ -20,9 +22,10 @@
 // the weights are not rounded to bf16.
 //
 // Determinism: every row's arithmetic depends only on its own position: the
-// block split is fixed by absolute position, masked keys have weight exactly
-// 0, keys past the last one any row of the group sees are zero-filled in
-// shared memory, and each output element of an mma depends only on its own
+// unit and sub-block split is fixed by absolute position, masked keys have
+// weight exactly 0 (a sub-block past a row leaves its running values
+// unchanged), keys past the last one any row of the group sees are zero-filled
+// in shared memory, and each output element of an mma depends only on its own
 // row of P.  A row gives the same bits alone or beside other rows (one-row
 // steps == windows, solo == batched).
 #include "common.cuh"
@@ -34,21 +37,19 @@ namespace tfl {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kWarps = attn::kWarps;
-constexpr int kRB = 4;               // rows per CTA
-constexpr int kKB = attn::kKB;
-constexpr int kMaxPairs = attn::kMaxPairs;
-constexpr int kMergeSlices = attn::kMergeSlices;
+constexpr int kRB = attn::kGroupRows;  // rows per CTA
+constexpr int kSub = attn::kSub;
+constexpr int kUnit = attn::kUnit;
 using attn::swz;
 
-// 75,776 bytes: three CTAs per SM.  The softmax weights (hi and lo parts,
-// 2 x 32 x 128 bf16) reuse the key tile once the scores are computed.
+// 201,728 bytes (one CTA per SM): queries, two buffers of one sub-block's
+// keys and values each (sub-block j+1 streams in while j is computed), and the
+// scratch that combines the eight warp partials.
 struct Smem {
-    bf16 q[kMaxPairs * kHeadDim];    // 8 KB
-    bf16 k[kKB * kHeadDim];          // 32 KB (then the weights)
-    bf16 v[kKB * kHeadDim];          // 32 KB
-    float wmax[kWarps][kMaxPairs];   // per-warp row maxima
-    float wsum[kWarps][kMaxPairs];   // per-warp row sums
+    bf16 q[attn::kPairs * kHeadDim];     // 4 KB
+    bf16 k[2][kSub * kHeadDim];          // 2 x 32 KB
+    bf16 v[2][kSub * kHeadDim];          // 2 x 32 KB
+    float comb[attn::kCombFloats];       // 65 KB
 };
 
 using wm::cp_async16_zfill;
@@ -71,57 +72,96 @@ __device__ __forceinline__ bool find_group(const RowMap& m, int z, int& s, int& 
     return false;
 }
 
+// Sub-block staging through cp.async, two buffers (see attn::unit_partial for
+// the contract): sub-block j lands in buffer j % 2 as one copy group; keys
+// past the last visible one are zero-filled.
+struct CpSrc {
+    Smem* sm;
+    const KvView* kv;
+    int layer, n_kv, g, k0, p_last, nsub, issued;
+    __device__ __forceinline__ void load(int j) {
+        const int kj = k0 + j * kSub;
+        const int nv = min(kSub, p_last + 1 - kj);
+        const bf16* kbase = kv_row(*kv, layer, 0, kj, n_kv) + (size_t)g * kHeadDim;
+        const bf16* vbase = kv_row(*kv, layer, 1, kj, n_kv) + (size_t)g * kHeadDim;
+        const size_t pstride = (size_t)n_kv * kHeadDim;
+        bf16* kd = sm->k[j & 1];
+        bf16* vd = sm->v[j & 1];
+        for (int i = threadIdx.x; i < kSub * 16; i += kThreads) {
+            const int t = i >> 4, c = i & 15;
+            const bool valid = t < nv;
+            const size_t off = valid ? t * pstride + c * 8 : 0;
+            cp_async16_zfill(kd + swz(t, c * 8), kbase + off, valid);
+            cp_async16_zfill(vd + swz(t, c * 8), vbase + off, valid);
+        }
+        cp_async_commit();
+        ++issued;
+    }
+    __device__ __forceinline__ uint32_t k(int j, int row, int col) const {
+        return smem_u32(sm->k[j & 1]) + 2u * swz(row, col);
+    }
+    __device__ __forceinline__ uint32_t v(int j, int row, int col) const {
+        return smem_u32(sm->v[j & 1]) + 2u * swz(row, col);
+    }
+    __device__ __forceinline__ void wait(int j) {
+        if (issued > j + 1)
+            cp_async_wait<1>();
+        else
+            cp_async_wait<0>();
+        __syncthreads();
+    }
+    __device__ __forceinline__ void done(int j) {
+        if (j + 2 < nsub) {
+            __syncthreads();  // every warp is done with buffer j % 2
+            load(j + 2);
+        }
+    }
+};
+
 // G = query heads per KV head.  Pair p = i*G + j is (row i of the group, head g*G + j).
 template <int G>
-__global__ void __launch_bounds__(kThreads, 3) attn_block_kernel(const __grid_constant__ AttnDecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) attn_block_kernel(const __grid_constant__ AttnDecodeArgs a) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
 
     int s, r0, nr;
     if (!find_group(a.rows, blockIdx.z, s, r0, nr)) return;
-    const int b = blockIdx.x, g = blockIdx.y;
+    const int u = blockIdx.x, g = blockIdx.y;
     const int p_first = a.rows.pos0[s] + (r0 - a.rows.row_start[s]);
     const int p_last = p_first + nr - 1;
-    const int k0 = b * kKB;
+    const int k0 = u * kUnit;
     if (k0 > p_last) return;
-    const int nv = min(kKB, p_last + 1 - k0);  // keys of this block any row sees
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int gq = lane >> 2, tig = lane & 3;
-    const int P = nr * G;
-    const int MT = (P + 15) / 16;  // m16 tiles of pairs
+    const int tid = threadIdx.x;
+    const int P = nr * G;  // (row, head) pairs, at most 16
 
-    // stage keys and values of head g (rows of 256 B inside one page); keys past
-    // nv are zero-filled so that their weight-0 products stay exact zeros.  Keys
-    // first, values second, as two copy groups.
-    const KvView& kv = a.rows.kv[s];
-    const bf16* kbase = kv_row(kv, a.layer, 0, k0, a.n_kv) + (size_t)g * kHeadDim;
-    const bf16* vbase = kv_row(kv, a.layer, 1, k0, a.n_kv) + (size_t)g * kHeadDim;
-    const size_t pstride = (size_t)a.n_kv * kHeadDim;
-    auto stage = [&](bf16* dst, const bf16* src) {
-        for (int i = tid; i < kKB * 16; i += kThreads) {
-            const int t = i >> 4, c = i & 15;
-            const bool valid = t < nv;
-            cp_async16_zfill(dst + swz(t, c * 8), src + (valid ? t * pstride + c * 8 : 0), valid);
-        }
-        cp_async_commit();
-    };
-    // A block whose keys all precede the stream's first row of this call holds
+    CpSrc src;
+    src.sm = &sm;
+    src.kv = &a.rows.kv[s];
+    src.layer = a.layer;
+    src.n_kv = a.n_kv;
+    src.g = g;
+    src.k0 = k0;
+    src.p_last = p_last;
+    src.nsub = min(4, (p_last - k0) / kSub + 1);
+    src.issued = 0;
+    // A unit whose keys all precede the stream's first row of this call holds
     // cache rows written by earlier calls (every kernel of the library signals
     // its dependents only after its own dependency wait, so those writers have
-    // completed): it streams in while the previous kernel is still finishing.
-    const bool early = k0 + nv <= a.rows.pos0[s];
+    // completed): its first sub-blocks stream in while the previous kernel is
+    // still finishing.
+    const bool early = k0 + src.nsub * kSub <= a.rows.pos0[s];
     if (early) {
-        stage(sm.k, kbase);
-        stage(sm.v, vbase);
+        src.load(0);
+        if (src.nsub > 1) src.load(1);
     }
     pdl_wait();
     pdl_trigger();
     if (!early) {
-        stage(sm.k, kbase);
-        stage(sm.v, vbase);
+        src.load(0);
+        if (src.nsub > 1) src.load(1);
     }
     // queries (bf16, unscaled); pairs past P are zero
-    for (int i = tid; i < MT * 16 * 16; i += kThreads) {
+    for (int i = tid; i < attn::kPairs * 16; i += kThreads) {
         const int p = i >> 4, c = i & 15;
         uint4 val = make_uint4(0u, 0u, 0u, 0u);
         if (p < P) {
@@ -131,42 +171,25 @@ __global__ void __launch_bounds__(kThreads, 3) attn_block_kernel(const __grid_co
         }
         *reinterpret_cast<uint4*>(&sm.q[swz(p, c * 8)]) = val;
     }
-    cp_async_wait<1>();  // the keys have landed; the values may still be in flight
-    __syncthreads();
-
-    attn::BlockGeom bg;
-    bg.b = b;
-    bg.g = g;
-    bg.r0 = r0;
-    bg.P = P;
-    bg.MT = MT;
-    bg.k0 = k0;
-    bg.nv = nv;
-    bg.p_first = p_first;
-    const uint32_t k_u = smem_u32(sm.k), v_u = smem_u32(sm.v);
-    attn::block_partial<G>(
-        a, bg, smem_u32(sm.q), k_u, sm.wmax, sm.wsum,
-        [&](int row, int col) { return k_u + 2u * swz(row, col); },
-        [&](int row, int col) { return v_u + 2u * swz(row, col); }, [] { __syncthreads(); },
-        [] {
-            cp_async_wait<0>();  // the values
-            __syncthreads();
-        });
+    __syncthreads();  // the queries
+    attn::UnitGeom ug;
+    ug.u = u;
+    ug.g = g;
+    ug.r0 = r0;
+    ug.P = P;
+    ug.k0 = k0;
+    ug.nsub = src.nsub;
+    ug.p_first = p_first;
+    ug.p_last = p_last;
+    attn::unit_partial<G>(a, ug, smem_u32(sm.q), sm.comb, src, [] { __syncthreads(); });
 }
 
-// One CTA per (head, row), kMergeSlices x 128 threads: thread (slice i, dim d)
-// folds blocks i, i + 8, i + 16, ... in order, all its loads issued ahead; the
-// eight slice sums are then added in slice order.  The fold depends only on
-// the row's position (its block count), never on the other rows of the call.
-__global__ void __launch_bounds__(kHeadDim* kMergeSlices) attn_merge_kernel(const __grid_constant__ AttnDecodeArgs a) {
-    constexpr int kT = kHeadDim * kMergeSlices;
-    __shared__ float wts[1024];
-    __shared__ float red[kT / 32];
-    __shared__ float so[kMergeSlices][kHeadDim];
-    __shared__ float sl[kMergeSlices];
+// One CTA of 128 threads (one per dim) per (head, row): the fold of
+// attn::merge128.
+__global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const __grid_constant__ AttnDecodeArgs a) {
     pdl_wait();
     pdl_trigger();
-    attn::merge<kT>(a, blockIdx.y, blockIdx.x, threadIdx.x, wts, red, so, sl, [] { __syncthreads(); });
+    attn::merge128(a, blockIdx.y, blockIdx.x, threadIdx.x);
 }
 
 }  // namespace
@@ -186,7 +209,7 @@ int attn_decode_blocks(const AttnDecodeArgs& a, int* groups) {
         max_pos = max(max_pos, a.rows.pos0[s] + rows - 1);
     }
     *groups = g;
-    return max_pos / kKB + 1;
+    return max_pos / kUnit + 1;
 }
 
 cudaError_t launch_attn_block(const AttnDecodeArgs& a, cudaStream_t st, bool pdl) {
@@ -214,7 +237,7 @@ cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t c2 = {};
     c2.gridDim = dim3(a.n_q, a.rows.n_rows);
-    c2.blockDim = dim3(kHeadDim * kMergeSlices);
+    c2.blockDim = dim3(kHeadDim);
     c2.stream = st;
     c2.attrs = attr;
     c2.numAttrs = pdl ? 1 : 0;

@@ -11,7 +11,8 @@ namespace tfl {
 typedef __nv_bfloat16 bf16;
 
 constexpr int kHeadDim = 128;      // D: the only head size the library serves
-constexpr int kPage = 128;         // KV positions per page (== decode key block)
+constexpr int kPage = 128;          // KV positions per page
+constexpr int kAttnUnit = 4 * kPage;  // keys per decode-attention partial (512)
 constexpr int kMaxStreams = 16;    // streams in one decode step
 constexpr int kMaxDecodeRows = 64; // rows in one decode step, over all streams
 constexpr int kMaxChunkRows = 2048;

@@ -76,13 +76,13 @@ extern "C" int tfl_attention_decode_noalloc(tfl_kv* kv, int layer, int pos0, int
         set_last_error(msg);
         return TFL_E_ARG;
     }
-    const int nblk = (pos0 + rows - 1) / kPage + 1;
+    const int nblk = (pos0 + rows - 1) / kAttnUnit + 1;
     const size_t units = (size_t)rows * n_q * nblk;
     if (units > kMaxUnits) {
         snprintf(msg, sizeof msg,
-                 "tfl_attention_decode_noalloc: %d rows x %d heads x %d key blocks of %d positions need %zu "
+                 "tfl_attention_decode_noalloc: %d rows x %d heads x %d key units of %d positions need %zu "
                  "partials; the fixed scratch holds %zu (16 MiB); use tfl_decode_step or tfl_layer_op instead",
-                 rows, n_q, nblk, kPage, units, kMaxUnits);
+                 rows, n_q, nblk, kAttnUnit, units, kMaxUnits);
         set_last_error(msg);
         return TFL_E_WORKSPACE;
     }

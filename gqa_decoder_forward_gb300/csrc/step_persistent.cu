@@ -11,7 +11,8 @@
 // The producer walks the same sequence as the consumers and keeps a ring of
 // eight 16 KB shared-memory stages full: the weight stages of the projections
 // and the key/value tiles of the attention units (128 positions x 64 dims per
-// stage, four stages per unit) stream in while the consumers are still at a
+// stage, four stages per 128-key sub-block, up to four sub-blocks per unit of
+// 512 keys) stream in while the consumers are still at a
 // barrier, so each phase starts with data in place instead of paying a
 // launch, a pipeline fill and a tail.  Only the key/value block holding this
 // step's own rows waits for the barrier after the QKV phase.
@@ -118,26 +119,27 @@ __device__ __forceinline__ int phase_tiles(const MatvecArgs& e) {
     return e.n_out / 16;
 }
 
-// Attention unit u of the step (the decode kernels' grid: key block, KV head,
-// group of up to four rows of one stream); false when the block lies past
-// every row of its group.  late: the block holds positions written this step.
+// Attention unit u of the step (the decode kernels' grid: 512-key unit, KV
+// head, group of up to two rows of one stream); false when the unit lies past
+// every row of its group.  nsub: its 128-key sub-blocks that any row sees.
+// late: it reaches positions written this step.
 struct Unit {
-    int s, b, g, r0, nr, p_first, k0, nv;
+    int s, b, g, r0, nr, p_first, p_last, k0, nsub;
     bool late;
 };
-__device__ __forceinline__ bool attn_unit(const StepArgs& a, int u, int nblk, Unit& x) {
-    x.b = u % nblk;
-    const int rest = u / nblk;
+__device__ __forceinline__ bool attn_unit(const StepArgs& a, int u, int nunits, Unit& x) {
+    x.b = u % nunits;
+    const int rest = u / nunits;
     x.g = rest % a.n_kv;
     int z = rest / a.n_kv;
     bool found = false;
     for (int t = 0; t < a.rows.n_streams && !found; ++t) {
         const int rows = a.rows.row_start[t + 1] - a.rows.row_start[t];
-        const int ng = (rows + 3) / 4;
+        const int ng = (rows + attn::kGroupRows - 1) / attn::kGroupRows;
         if (z < ng) {
             x.s = t;
-            x.r0 = a.rows.row_start[t] + z * 4;
-            x.nr = min(4, rows - z * 4);
+            x.r0 = a.rows.row_start[t] + z * attn::kGroupRows;
+            x.nr = min(attn::kGroupRows, rows - z * attn::kGroupRows);
             found = true;
         } else {
             z -= ng;
@@ -145,11 +147,11 @@ __device__ __forceinline__ bool attn_unit(const StepArgs& a, int u, int nblk, Un
     }
     if (!found) return false;
     x.p_first = a.rows.pos0[x.s] + (x.r0 - a.rows.row_start[x.s]);
-    const int p_last = x.p_first + x.nr - 1;
-    x.k0 = x.b * kPage;
-    if (x.k0 > p_last) return false;
-    x.nv = min(kPage, p_last + 1 - x.k0);
-    x.late = x.k0 + x.nv > a.rows.pos0[x.s];
+    x.p_last = x.p_first + x.nr - 1;
+    x.k0 = x.b * kAttnUnit;
+    if (x.k0 > x.p_last) return false;
+    x.nsub = min(4, (x.p_last - x.k0) / kPage + 1);
+    x.late = x.k0 + x.nsub * kPage > a.rows.pos0[x.s];
     return true;
 }
 
@@ -157,12 +159,13 @@ __device__ __forceinline__ int attn_blocks(const StepArgs& a) {
     int max_pos = 0;
     for (int s = 0; s < a.rows.n_streams; ++s)
         max_pos = max(max_pos, a.rows.pos0[s] + a.rows.row_start[s + 1] - a.rows.row_start[s] - 1);
-    return max_pos / kPage + 1;
+    return max_pos / kAttnUnit + 1;
 }
 
 __device__ __forceinline__ int attn_groups(const StepArgs& a) {
     int g = 0;
-    for (int s = 0; s < a.rows.n_streams; ++s) g += (a.rows.row_start[s + 1] - a.rows.row_start[s] + 3) / 4;
+    for (int s = 0; s < a.rows.n_streams; ++s)
+        g += (a.rows.row_start[s + 1] - a.rows.row_start[s] + attn::kGroupRows - 1) / attn::kGroupRows;
     return g;
 }
 
@@ -241,13 +244,15 @@ __device__ void producer(const StepArgs& a, unsigned char* ring, uint64_t* full,
                     waited = true;
                 }
                 const KvView& kv = a.rows.kv[x.s];
-                const int page = __ldg(kv.table + x.b);
-                for (int part = 0; part < 4; ++part) {  // K dims 0-63, K 64-127, V 0-63, V 64-127
-                    unsigned char* dst = take();
-                    if (!dst) return;
-                    const int row0 = ((l * 2 + (part >> 1)) * kv.n_pages + page) * kPage;
-                    tma_load_3d(dst, &a.kvmap[x.s], (part & 1) * 64, x.g, row0, &full[rp.stage], pol);
-                    rp.advance();
+                for (int j = 0; j < x.nsub; ++j) {
+                    const int page = __ldg(kv.table + x.k0 / kPage + j);
+                    for (int part = 0; part < 4; ++part) {  // K dims 0-63, K 64-127, V 0-63, V 64-127
+                        unsigned char* dst = take();
+                        if (!dst) return;
+                        const int row0 = ((l * 2 + (part >> 1)) * kv.n_pages + page) * kPage;
+                        tma_load_3d(dst, &a.kvmap[x.s], (part & 1) * 64, x.g, row0, &full[rp.stage], pol);
+                        rp.advance();
+                    }
                 }
             }
         if (!weights(l, PH_O) || !weights(l, PH_GATEUP) || !weights(l, PH_DOWN)) return;
@@ -256,19 +261,78 @@ __device__ void producer(const StepArgs& a, unsigned char* ring, uint64_t* full,
 }
 
 // ---- consumers (warps 0..7) ------------------------------------------------------
+// Sub-block source over the ring (see attn::unit_partial): sub-block j of the
+// unit is stages 4j .. 4j+3 after the unit's first (K lo, K hi, V lo, V hi),
+// written by TMA with 128-byte swizzle (row r = a position, 64 dims).
+struct RingSrc {
+    unsigned char* ring;
+    uint64_t* full;
+    uint64_t* empty;
+    RingPos base;
+    int* status;
+    volatile int* s_abort;
+    int k0, p_last;
+    __device__ __forceinline__ RingPos at(int i) const {
+        RingPos r;
+        r.stage = (base.stage + i) % kDepth;
+        r.phase = base.phase ^ (uint32_t)(((base.stage + i) / kDepth) & 1);
+        return r;
+    }
+    __device__ __forceinline__ uint32_t addr(int i) const { return smem_u32(ring + at(i).stage * kStage); }
+    __device__ __forceinline__ static uint32_t tile(uint32_t lo, uint32_t hi, int row, int col) {
+        return (col < 64 ? lo : hi) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4);
+    }
+    __device__ __forceinline__ uint32_t k(int j, int row, int col) const {
+        return tile(addr(4 * j), addr(4 * j + 1), row, col);
+    }
+    __device__ __forceinline__ uint32_t v(int j, int row, int col) const {
+        return tile(addr(4 * j + 2), addr(4 * j + 3), row, col);
+    }
+    __device__ __forceinline__ void wait_stage(int i) const {
+        const RingPos r = at(i);
+        if (!*s_abort && !mbar_wait(&full[r.stage], r.phase, status)) *s_abort = 1;
+    }
+    __device__ __forceinline__ void release(int i) const {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[at(i).stage]);
+    }
+    // this warp's key rows 16w..16w+15: values past the last visible key become
+    // exact zeros (their weight is 0, and the cache there holds anything)
+    __device__ __forceinline__ void wait(int j) {
+        for (int i = 0; i < 4; ++i) wait_stage(4 * j + i);
+        const int nv = min(kPage, p_last + 1 - (k0 + j * kPage));
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int r0 = max(nv, w * 16), r1 = w * 16 + 16;
+        if (r0 < r1) {
+            const uint32_t v0 = addr(4 * j + 2), v1 = addr(4 * j + 3);
+            for (int i = lane; i < (r1 - r0) * 8 * 2; i += 32) {
+                const int half = i >= (r1 - r0) * 8;
+                const int c = half ? i - (r1 - r0) * 8 : i;
+                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"((half ? v1 : v0) + r0 * 128 + c * 16),
+                             "r"(0u)
+                             : "memory");
+            }
+            // the stage is refilled by TMA later: order these generic writes before it
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+        }
+    }
+    __device__ __forceinline__ void done(int j) {
+        for (int i = 0; i < 4; ++i) release(4 * j + i);
+    }
+};
+
 template <int GQ>
 __device__ __forceinline__ void attention_unit(const StepArgs& a, const AttnDecodeArgs& at, const Unit& x,
-                                               unsigned char* ring, unsigned char* xs, uint64_t* full, RingPos rp,
-                                               volatile int* s_abort) {
+                                               unsigned char* ring, unsigned char* xs, uint64_t* full, uint64_t* empty,
+                                               RingPos rp, volatile int* s_abort) {
     const int tid = threadIdx.x;
     const ConsumerBar bar;
-    const int P = x.nr * GQ, MT = (P + 15) / 16;
-    const uint32_t xs_u = smem_u32(xs);
-    const uint32_t q_u = xs_u, p_u = xs_u + attn::kMaxPairs * kHeadDim * 2;
-    float(*wmax)[attn::kMaxPairs] = reinterpret_cast<float(*)[attn::kMaxPairs]>(xs + 3 * attn::kMaxPairs * kHeadDim * 2);
-    float(*wsum)[attn::kMaxPairs] = wmax + attn::kWarps;
+    const int P = x.nr * GQ;
+    const uint32_t q_u = smem_u32(xs);
+    float* comb = reinterpret_cast<float*>(xs + attn::kPairs * kHeadDim * 2);
     // queries of the group's (row, head) pairs; pairs past P are zero
-    for (int i = tid; i < MT * 16 * 16; i += kConsumerWarps * 32) {
+    for (int i = tid; i < attn::kPairs * 16; i += kConsumerWarps * 32) {
         const int p = i >> 4, c = i & 15;
         uint4 val = make_uint4(0u, 0u, 0u, 0u);
         if (p < P) {
@@ -279,50 +343,26 @@ __device__ __forceinline__ void attention_unit(const StepArgs& a, const AttnDeco
                      "r"(val.y), "r"(val.z), "r"(val.w)
                      : "memory");
     }
-    RingPos s[4];
-    s[0] = rp;
-    for (int j = 1; j < 4; ++j) {
-        s[j] = s[j - 1];
-        s[j].advance();
-    }
-    for (int j = 0; j < 2; ++j)
-        if (!*s_abort && !mbar_wait(&full[s[j].stage], s[j].phase, a.status)) *s_abort = 1;
     bar();
-    // stage tiles written by TMA with 128-byte swizzle: row r (a position), 64 dims
-    const uint32_t k0u = smem_u32(ring + s[0].stage * kStage), k1u = smem_u32(ring + s[1].stage * kStage);
-    const uint32_t v0u = smem_u32(ring + s[2].stage * kStage), v1u = smem_u32(ring + s[3].stage * kStage);
-    auto tile_addr = [](uint32_t lo, uint32_t hi, int row, int col) {
-        return (col < 64 ? lo : hi) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4);
-    };
-    attn::BlockGeom bg;
-    bg.b = x.b;
-    bg.g = x.g;
-    bg.r0 = x.r0;
-    bg.P = P;
-    bg.MT = MT;
-    bg.k0 = x.k0;
-    bg.nv = x.nv;
-    bg.p_first = x.p_first;
-    attn::block_partial<GQ>(
-        at, bg, q_u, p_u, wmax, wsum, [&](int row, int col) { return tile_addr(k0u, k1u, row, col); },
-        [&](int row, int col) { return tile_addr(v0u, v1u, row, col); }, bar,
-        [&] {
-            for (int j = 2; j < 4; ++j)
-                if (!*s_abort && !mbar_wait(&full[s[j].stage], s[j].phase, a.status)) *s_abort = 1;
-            if (x.nv < kPage) {
-                // values past the last visible key must be exact zeros (their weight is 0)
-                const int n16 = (kPage - x.nv) * 8;  // 16-byte chunks per stage
-                for (int i = tid; i < 2 * n16; i += kConsumerWarps * 32) {
-                    const uint32_t base = i < n16 ? v0u : v1u;
-                    const int c = i < n16 ? i : i - n16;
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(base + x.nv * 128 + c * 16), "r"(0u)
-                                 : "memory");
-                }
-                // the stage is refilled by TMA later: order these generic writes before it
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            }
-            bar();
-        });
+    RingSrc src;
+    src.ring = ring;
+    src.full = full;
+    src.empty = empty;
+    src.base = rp;
+    src.status = a.status;
+    src.s_abort = s_abort;
+    src.k0 = x.k0;
+    src.p_last = x.p_last;
+    attn::UnitGeom ug;
+    ug.u = x.b;
+    ug.g = x.g;
+    ug.r0 = x.r0;
+    ug.P = P;
+    ug.k0 = x.k0;
+    ug.nsub = x.nsub;
+    ug.p_first = x.p_first;
+    ug.p_last = x.p_last;
+    attn::unit_partial<GQ>(at, ug, q_u, comb, src, bar);
 }
 
 __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char* xs, float* red, float* red_norm,
@@ -399,30 +439,15 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
                 if (!attn_unit(a, u, nblk, x) || (int)x.late != pass) continue;
                 bar();  // the previous unit is done with the queries and weights
                 if (GQ == 7)
-                    attention_unit<7>(a, at, x, ring, xs, full, rp, s_abort);
+                    attention_unit<7>(a, at, x, ring, xs, full, empty, rp, s_abort);
                 else
-                    attention_unit<8>(a, at, x, ring, xs, full, rp, s_abort);
-                __syncwarp();
-                if (lane == 0)
-                    for (int j = 0; j < 4; ++j) {
-                        mbar_arrive(&empty[rp.stage]);
-                        rp.advance();
-                    }
-                else
-                    for (int j = 0; j < 4; ++j) rp.advance();
+                    attention_unit<8>(a, at, x, ring, xs, full, empty, rp, s_abort);
+                for (int j = 0; j < 4 * x.nsub; ++j) rp.advance();
             }
         if (!grid_barrier()) return;
-        // merge: one (row, head) per unit
-        {
-            float* wts = reinterpret_cast<float*>(xs);
-            float* redm = wts + 1024;
-            float(*so)[kHeadDim] = reinterpret_cast<float(*)[kHeadDim]>(wts + 1024 + 16);
-            float* sl = wts + 1024 + 16 + attn::kMergeSlices * kHeadDim;
-            for (int u = blockIdx.x; u < R * a.n_q; u += G) {
-                bar();
-                attn::merge<kConsumerWarps * 32>(at, u / a.n_q, u % a.n_q, tid, wts, redm, so, sl, bar);
-            }
-        }
+        // merge: one (row, head) per 128 threads
+        for (int u = blockIdx.x * 2 + (tid >> 7); u < R * a.n_q; u += 2 * G)
+            attn::merge128(at, u / a.n_q, u % a.n_q, tid & (kHeadDim - 1));
         if (!grid_barrier()) return;
         matvec(l, PH_O, aorow, nullptr);
         if (!grid_barrier()) return;

@@ -54,6 +54,15 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Transpose of an 8x8 b16 matrix held in the mma fragment layout (thread
+// (g, t) holds row g, columns 2t and 2t+1): afterwards it holds row g of the
+// transpose, i.e. column g, rows 2t and 2t+1 of the original.
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 // Two bf16 in one register: lo in bits 0..15 (the lower column), hi in 16..31.
 __device__ __forceinline__ uint32_t pack_bf16(bf16 lo, bf16 hi) {
     return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);

@@ -302,8 +302,8 @@ int tfl_layer_op(tfl_model* model, int op, int layer, tfl_kv* kv, int pos0, int 
  * pos0+rows-1 attend keys 0..pos0+i of kv (layer); out is device bf16
  * [rows][n_q*D].  The softmax partials live in a fixed 16 MiB array inside the
  * library (held on every GPU that loads it until the process exits):
- * rows * n_q * ceil((pos0+rows)/128) must not exceed 32,263 (for the 33B shape:
- * one row up to 73,728 positions, 16 rows up to 4,608), else TFL_E_WORKSPACE
+ * rows * n_q * ceil((pos0+rows)/512) must not exceed 32,263 (for the 33B shape:
+ * one row up to 294,912 positions, 16 rows up to 18,432), else TFL_E_WORKSPACE
  * with a message.  The first call on each device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.  All calls share the array: calls that overlap on

@@ -55,10 +55,10 @@ def test_noalloc_attention_matches_workspace_attention_twice(shape):
 
 def test_noalloc_attention_refuses_sizes_beyond_its_scratch():
     shape = synth.NANBEIGE_33B.with_layers(1)
-    m = _attention_only_model(shape, 8192)
-    kv = m.kv(8192)
+    m = _attention_only_model(shape, 20480)
+    kv = m.kv(20480)
     q = torch.zeros((16, shape.n_q * 128), dtype=torch.bfloat16, device="cuda")
     out = torch.empty_like(q)
     with pytest.raises(tfl.TflError) as e:
-        tfl.tfl_attention_decode_noalloc(kv, 0, 8000, q, out)   # 16 rows x 56 heads x 63 blocks
+        tfl.tfl_attention_decode_noalloc(kv, 0, 20000, q, out)   # 16 rows x 56 heads x 40 units of 512 keys
     assert e.value.code == tfl.TFL_E_WORKSPACE and "16 MiB" in str(e.value)
