@@ -359,6 +359,10 @@ def run_tfl(args, world, rank, local):
     for _ in range(prof_steps):
         step()
     prof = tfl.tfl_profile_read(model)
+    try:
+        phases = tfl.tfl_step_phases(model)   # the last profiled step, when it ran persistent
+    except tfl.TflError:
+        phases = None
     tfl.tfl_profile(model, False)
     launches_per_step = sum(n for _, n in prof.values()) / prof_steps
 
@@ -443,6 +447,7 @@ def run_tfl(args, world, rank, local):
         "kernels": {k: {"ms_per_step": round(v[0] / prof_steps, 4), "launches_per_step": v[1] / prof_steps}
                     for k, v in prof.items() if v[1]},
         "per_launch_path_ms_per_step": round(per_launch_ms, 4),
+        "step_phases_us": phases,
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "e2e": {"value": round(world / e2e_s, 3), "unit": "tok/s", "h2d_bytes_per_step": 4,
                 "d2h_bytes_per_step": 4},

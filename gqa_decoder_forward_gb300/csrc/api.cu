@@ -8,6 +8,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <algorithm>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -90,7 +91,7 @@ int qualify(const tfl_config* c) {
 
 // Workspace layout (byte offsets, 256-byte aligned regions).
 struct Layout {
-    size_t h, xn, q, ao, act, pm, pl, po, cos_t, sin_t, status, wmaps, norms, sync, zero, total;
+    size_t h, xn, q, ao, act, pm, pl, po, cos_t, sin_t, status, wmaps, norms, sync, zero, ts, total;
     int max_blocks;
 };
 
@@ -124,6 +125,7 @@ Layout layout(const tfl_config* c) {
     L.norms = take((size_t)c->layers * 2 * sizeof(void*));
     L.sync = take(256);
     L.zero = take((size_t)c->hidden * 2);
+    L.ts = take((size_t)kStepTsCtas * step_ts_stride(c->layers) * 8);
     L.total = off;
     return L;
 }
@@ -252,6 +254,8 @@ struct tfl_model {
     const bf16** d_norms;   // workspace copy of the norm weight pointers
     unsigned* sync;
     bf16* zero_row;
+    unsigned long long* ts;  // decode-step phase stamps (written while profiling)
+    bool ts_valid = false;
     bool persistent = true; // decode steps of <= kStepMaxRows rows as one launch
     bool pdl;
     // TMA descriptors of every projection and of the activation buffers
@@ -533,7 +537,9 @@ int run_step_persistent(tfl_model* m, tfl_kv* const* kvs, const RowMap& rm, cons
     a.logits = (bf16*)logits;
     a.rows = rm;
     for (int s = 0; s < rm.n_streams; ++s) a.kvmap[s] = kvs[s]->kvmap;
+    a.ts = (m->prof && m->grid <= kStepTsCtas) ? m->ts : nullptr;
     LAUNCH(m, K_STEP, st, launch_step_persistent(a, m->grid, st));
+    if (a.ts) m->ts_valid = true;
     return TFL_OK;
 }
 
@@ -811,6 +817,7 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
     m->d_norms = (const bf16**)(m->ws + L.norms);
     m->sync = (unsigned*)(m->ws + L.sync);
     m->zero_row = (bf16*)(m->ws + L.zero);
+    m->ts = (unsigned long long*)(m->ws + L.ts);
     m->pdl = true;
 
     // projections: TMA descriptors of every weight matrix and activation buffer
@@ -883,6 +890,31 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
 }
 
 void tfl_free(tfl_model* m) { delete m; }
+
+int tfl_step_phases(tfl_model* m, double* out, int n) {
+    if (!m || !out || n < 9) return fail(TFL_E_ARG, "NULL model or output, or n < 9");
+    if (!m->ts_valid) return fail(TFL_E_ARG, "no profiled persistent decode step since the last tfl_step_phases");
+    const int L = m->cfg.layers, stride = step_ts_stride(L), G = m->grid;
+    std::vector<unsigned long long> t((size_t)G * stride);
+    CK(cudaDeviceSynchronize());
+    CK(cudaMemcpy(t.data(), m->ts, t.size() * 8, cudaMemcpyDeviceToHost));
+    m->ts_valid = false;
+    auto at = [&](int c, int i) { return (double)t[(size_t)c * stride + i]; };
+    auto cmax = [&](int i) { double v = at(0, i); for (int c = 1; c < G; ++c) v = std::max(v, at(c, i)); return v; };
+    auto cmin = [&](int i) { double v = at(0, i); for (int c = 1; c < G; ++c) v = std::min(v, at(c, i)); return v; };
+    for (int k = 0; k < 9; ++k) out[k] = 0.0;
+    double prev = cmax(0), bar_sum = 0.0;
+    for (int e = 1; e <= 6 * L; ++e) {
+        const double pass = cmax(2 * e + 1);
+        out[(e - 1) % 6] += (pass - prev) / 1e3 / L;
+        bar_sum += (cmin(2 * e + 1) - cmax(2 * e)) / 1e3;
+        prev = pass;
+    }
+    out[6] = bar_sum / (6.0 * L);
+    out[7] = (cmax(1) - prev) / 1e3;
+    out[8] = (cmax(1) - cmin(0)) / 1e3;
+    return ok();
+}
 
 int tfl_set_persistent(tfl_model* m, int enable) {
     if (!m) return fail(TFL_E_ARG, "NULL model");

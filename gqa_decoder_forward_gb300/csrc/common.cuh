@@ -179,8 +179,13 @@ struct StepArgs {
     const int32_t* ids;         // device, n_rows
     bf16* logits;               // device [n_rows][V]
     RowMap rows;
+    unsigned long long* ts;     // optional (NULL: off): per CTA, kStepTsStride global-timer stamps
     CUtensorMap kvmap[kStepMaxRows];  // per stream: 3-D map over the cache pages (128 dims, n_kv, rows)
 };
+// Phase stamps of the decode-step kernel, per CTA: [0] start, [1] end, then for
+// grid barrier e = 1, 2, ...: [2e] arrival, [2e+1] pass.
+constexpr int kStepTsCtas = 160;
+__host__ __device__ inline int step_ts_stride(int layers) { return 2 + 2 * 6 * layers; }
 int step_smem_bytes();
 cudaError_t init_step_persistent();
 cudaError_t launch_step_persistent(const StepArgs& a, int grid, cudaStream_t st);

@@ -386,14 +386,24 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
     at.n_kv = a.n_kv;
     at.rows = a.rows;
 
+    unsigned long long* ts = a.ts ? a.ts + (size_t)blockIdx.x * step_ts_stride(a.layers) : nullptr;
+    auto stamp = [&](int i) {
+        if (ts && tid == 0) {
+            unsigned long long t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            ts[i] = t;
+        }
+    };
     auto grid_barrier = [&]() -> bool {
         bar();  // this CTA's writes of the phase are done
         ++epoch;
+        stamp(2 * epoch);
         if (tid == 0) {
             __threadfence();
             atomicAdd(a.sync, 1u);
             if (!wait_counter(a, epoch * (unsigned)G)) *s_abort = 1;
         }
+        stamp(2 * epoch + 1);
         bar();
         return !*s_abort;
     };
@@ -413,6 +423,7 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
         return (id >= 0 && id < a.V) ? a.embed + (size_t)id * a.H : a.zero_row;
     };
 
+    stamp(0);
     for (int l = 0; l < a.layers; ++l) {
         // RMSNorm + QKV + RoPE + KV append
         if (l == 0) {
@@ -457,6 +468,8 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
         if (!grid_barrier()) return;
     }
     matvec(0, PH_HEAD, hrow, a.final_norm);
+    bar();
+    stamp(1);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {

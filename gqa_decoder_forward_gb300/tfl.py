@@ -78,6 +78,7 @@ SIGNATURES = {
     "tfl_attention_decode_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp]),
     "tfl_profile": (ctypes.c_int, [_vp, ctypes.c_int]),
     "tfl_set_persistent": (ctypes.c_int, [_vp, ctypes.c_int]),
+    "tfl_step_phases": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_double), ctypes.c_int]),
     "tfl_profile_read": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_long)]),
     "tfl_profile_kind": (ctypes.c_char_p, [ctypes.c_int]),
@@ -309,6 +310,16 @@ def tfl_attention_decode_noalloc(kv: "KV", layer: int, pos0: int, q: torch.Tenso
 
 def tfl_profile(model: Model, enable: bool):
     return _check(lib().tfl_profile(model.handle, 1 if enable else 0))
+
+
+STEP_PHASES = ("qkv", "attention", "merge", "o", "gate_up", "down", "barrier", "head", "total")
+
+
+def tfl_step_phases(model: Model) -> dict:
+    """{phase: microseconds} of the last persistent decode step run while profiling."""
+    out = (ctypes.c_double * len(STEP_PHASES))()
+    _check(lib().tfl_step_phases(model.handle, out, len(STEP_PHASES)))
+    return {k: round(v, 3) for k, v in zip(STEP_PHASES, out)}
 
 
 def tfl_profile_read(model: Model) -> dict:

@@ -333,6 +333,18 @@ int tfl_profile(tfl_model* model, int enable);
 int tfl_profile_read(tfl_model* model, int n_kinds, double* ms, long* launches);
 const char* tfl_profile_kind(int kind);
 
+/*
+ * Phase times of the last persistent decode step run while profiling was on:
+ * out[0..5] the mean per layer (microseconds, from the last CTA leaving the
+ * previous grid barrier to the last CTA leaving this one) of the RMSNorm+QKV,
+ * attention, merge, o projection, RMSNorm+gate/up and down phases; out[6] the
+ * mean barrier latency (last arrival to first departure); out[7] the final
+ * norm + lm_head phase; out[8] the whole kernel.  n >= 9.  Synchronises the
+ * device.  TFL_E_ARG when no such step ran since the last call.  No
+ * counterpart on the pages (a measurement aid).
+ */
+int tfl_step_phases(tfl_model* model, double* out, int n);
+
 #ifdef __cplusplus
 }
 #endif

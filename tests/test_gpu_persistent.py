@@ -101,3 +101,21 @@ def test_persistent_bad_token_raises_status():
     m.decode_step([kv], torch.tensor([TINY.vocab + 5], dtype=torch.int32, device="cuda"), [1], lg)
     assert m.status() == tfl.TFL_E_ARG
     assert kv.length == 11
+
+
+def test_step_phases_are_reported_for_a_profiled_step():
+    w = gu.gpu_weights(TINY, 1)
+    m = tfl.Model(TINY, w, max_context=256, max_rows=64)
+    kv = m.kv(128)
+    m.prefill_chunk(kv, synth.uniform_ids(4, 40, TINY.vocab, "cuda"))
+    lg = torch.empty((1, TINY.vocab), dtype=torch.bfloat16, device="cuda")
+    tfl.tfl_profile(m, True)
+    m.decode_step([kv], synth.uniform_ids(5, 1, TINY.vocab, "cuda"), [1], lg)
+    ph = tfl.tfl_step_phases(m)
+    tfl.tfl_profile(m, False)
+    assert set(ph) == set(tfl.STEP_PHASES)
+    assert all(v >= 0 for v in ph.values())
+    per_layer = sum(ph[k] for k in ("qkv", "attention", "merge", "o", "gate_up", "down"))
+    assert 0 < per_layer * TINY.layers + ph["head"] <= ph["total"] * 1.001
+    with pytest.raises(tfl.TflError):   # read once per profiled step
+        tfl.tfl_step_phases(m)
