@@ -49,6 +49,9 @@ def parse():
                    help="time one decode op (qkv_rope, attention, o_residual, gate_up, down_residual, attn_norm) "
                         "on a one-layer 33B-shaped model instead of the full step")
     p.add_argument("--rows", type=int, default=1, help="rows per step for --op")
+    p.add_argument("--concurrent", type=int, default=0,
+                   help="time decode steps of this many streams (1 row each, seeded caches of --context "
+                        "positions) instead of the default line")
     p.add_argument("--prompt", action="store_true",
                    help="--op runs the prompt-chunk kernel of the op (rows up to 2,048)")
     return p.parse_args()
@@ -459,6 +462,63 @@ def run_tfl(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_concurrent(args):
+    """Decode steps of S streams x 1 row over seeded caches of --context positions each
+    (the concurrent configurations: 2 x 131,072 and 16 x 8,192)."""
+    from gqa_decoder_forward_gb300 import build, tfl
+    build.build()
+    S, ctx = args.concurrent, args.context
+    shape = SHAPE.with_layers(args.layers)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    weights = synth.model_weights(shape, 21, dev)
+    extra = args.warmup + args.steps + 9
+    model = tfl.Model(shape, weights, max_rows=64, max_decode_rows=64, max_context=ctx + extra)
+    kvs = [model.kv(ctx + extra) for _ in range(S)]
+    for l in range(shape.layers):
+        K, V = synth.kv_contents(shape, 22, l, ctx, dev)
+        for kv in kvs:
+            kv.write(l, 0, K, V)
+        del K, V
+    for kv in kvs:
+        kv.reset(ctx)
+    ids = synth.uniform_ids(41, S, shape.vocab, dev)
+    logits = torch.empty((S, shape.vocab), dtype=torch.bfloat16, device=dev)
+    st = torch.cuda.current_stream()
+
+    def step():
+        model.decode_step(kvs, ids, [1] * S, logits)
+        model.argmax(logits, ids)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clk:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(st)
+        for _ in range(args.steps):
+            step()
+        t1.record(st)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    phases = None
+    if S <= 2:
+        tfl.tfl_profile(model, True)
+        step()
+        tfl.tfl_profile_read(model)
+        phases = tfl.tfl_step_phases(model)
+        tfl.tfl_profile(model, False)
+    mean_ctx = ctx + args.warmup + (args.steps - 1) / 2.0
+    w = step_bytes(shape, 0)
+    kvb = shape.layers * 2 * shape.n_kv * shape.head_dim * 2 * mean_ctx * S
+    peak, peak_kind = measured_peaks()
+    gbs = (w + kvb) / (ms / 1e3) / 1e9
+    print(json.dumps({"mode": "concurrent", "streams": S, "context": ctx, "layers": args.layers,
+                      "path": "persistent" if S <= 2 else "launch per operation",
+                      "tok_s": round(S * 1e3 / ms, 2), "ms_per_step": round(ms, 4), "bytes_per_step": int(w + kvb),
+                      "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+                      "status": model.status(), "step_phases_us": phases, "clocks": clk.summary()}), flush=True)
+
+
 def run_op(args):
     """Times one decode op on a one-layer 33B-shaped model (a few GB on the device):
     the small case the kernel profiles are taken on."""
@@ -508,6 +568,9 @@ def main():
     args = parse()
     if args.op:
         run_op(args)
+        return
+    if args.concurrent:
+        run_concurrent(args)
         return
     world, rank, local = dist_init(args)
     if args.impl == "reference":

@@ -8,7 +8,8 @@
 // bf16, running sums, O = P V); the warp partials are then combined in warp
 // order.  Written per (row, head): m_u, l_u and o_u.
 // Merge: per (row, head), M = max_u m_u, then L = sum l_u 2^(m_u - M) and
-// O = sum o_u 2^(m_u - M) folded in unit order; out = bf16(O / L).
+// O = sum o_u 2^(m_u - M) folded in unit order over four contiguous quarters,
+// the quarters added in order; out = bf16(O / L).
 #pragma once
 
 #include "common.cuh"
@@ -36,7 +37,9 @@ constexpr int kSub = kPage;          // keys per sub-block
 constexpr int kUnit = kAttnUnit;     // keys per unit (one partial per (row, head, unit))
 constexpr int kGroupRows = 2;        // rows per group: G * 2 <= 16 (row, head) pairs, one m16 tile
 constexpr int kPairs = 16;
-constexpr int kCombFloats = kWarps * kPairs * kHeadDim + 2 * kWarps * kPairs;  // combine scratch
+constexpr int kCombFloats = kWarps * kPairs * kHeadDim + 2 * kWarps * kPairs;  // combine scratch (16 pairs)
+// floats of combine scratch for P pairs
+__host__ __device__ constexpr int comb_floats(int P) { return (kWarps * kHeadDim + 2 * kWarps) * ((P + 7) / 8) * 8; }
 
 struct UnitGeom {
     int u, g;        // unit, KV head
@@ -48,7 +51,7 @@ struct UnitGeom {
 
 // One unit partial by the eight warps (threads 0..255).  q_u: shared address
 // of the queries (16 pairs x 128 bf16, swz layout, pairs past P zero), visible
-// to every warp.  comb: kCombFloats floats of shared memory.  src provides,
+// to every warp.  comb: comb_floats(P) floats of shared memory.  src provides,
 // for sub-block j: wait(j) (this warp may read the sub-block's keys and
 // values; values past the last visible key are exact zeros), done(j) (this
 // warp has read its last key and value of j), k(j, row, col) / v(j, row, col)
@@ -194,9 +197,10 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
     }
 
     // ---- combine the eight warp partials (warp order) ----
+    constexpr int PS = NP * 8;                          // pair stride of the scratch
     float* co = comb;                                   // [warp][pair][dim]
-    float* cm = comb + kWarps * kPairs * kHeadDim;      // [warp][pair]
-    float* cl = cm + kWarps * kPairs;
+    float* cm = comb + kWarps * PS * kHeadDim;          // [warp][pair]
+    float* cl = cm + kWarps * PS;
 #pragma unroll
     for (int nt = 0; nt < NP; ++nt) {
 #pragma unroll
@@ -204,14 +208,14 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int p = nt * 8 + 2 * tig + e;
-                co[((size_t)warp * kPairs + p) * kHeadDim + dt * 16 + gq] = ot[dt][nt][e];
-                co[((size_t)warp * kPairs + p) * kHeadDim + dt * 16 + gq + 8] = ot[dt][nt][2 + e];
+                co[((size_t)warp * PS + p) * kHeadDim + dt * 16 + gq] = ot[dt][nt][e];
+                co[((size_t)warp * PS + p) * kHeadDim + dt * 16 + gq + 8] = ot[dt][nt][2 + e];
             }
         if (gq == 0) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                cm[warp * kPairs + nt * 8 + 2 * tig + e] = m_w[nt][e];
-                cl[warp * kPairs + nt * 8 + 2 * tig + e] = l_w[nt][e];
+                cm[warp * PS + nt * 8 + 2 * tig + e] = m_w[nt][e];
+                cl[warp * PS + nt * 8 + 2 * tig + e] = l_w[nt][e];
             }
         }
     }
@@ -220,15 +224,15 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
     for (int p = tid >> 7; p < P; p += 2) {
         float M = cm[p];
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, cm[w * kPairs + p]);
+        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, cm[w * PS + p]);
         float O = 0.f, L = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
-                const float mw = cm[w * kPairs + p];
+                const float mw = cm[w * PS + p];
                 const float aw = mw == -INFINITY ? 0.f : exp2f(mw - M);
-                O = fmaf(co[((size_t)w * kPairs + p) * kHeadDim + d], aw, O);
-                L = fmaf(cl[w * kPairs + p], aw, L);
+                O = fmaf(co[((size_t)w * PS + p) * kHeadDim + d], aw, O);
+                L = fmaf(cl[w * PS + p], aw, L);
             }
         }
         const int row = ug.r0 + p / G, head = ug.g * G + p % G;
@@ -251,20 +255,19 @@ __device__ __forceinline__ void unit_partial(const AttnDecodeArgs& a, const Unit
         unit_partial_np<G, 2>(a, ug, q_u, comb, src, bar);
 }
 
-// Merge of (row, head) over its units by 128 threads (thread = dim):
-// M = max_u m_u, then O = sum_u o_u 2^(m_u - M) and L = sum_u l_u 2^(m_u - M) as
-// fused multiply-adds in unit order; out = bf16(O / L).  The fold depends
-// only on the row's position (its unit count), never on the other rows.
-__device__ __forceinline__ void merge128(const AttnDecodeArgs& a, int row, int head, int d) {
-    const int s = row_stream(a.rows, row);
-    const int pos = a.rows.pos0[s] + (row - a.rows.row_start[s]);
-    const int nu = pos / kUnit + 1;
-    const size_t base = ((size_t)row * a.n_q + head) * a.max_blocks;
-    float M = -INFINITY;
-    for (int u = 0; u < nu; ++u) M = fmaxf(M, a.pm[base + u]);
+// Merge of (row, head) over its units: M = max_u m_u; the units are cut into
+// four contiguous quarters [q nu/4, (q+1) nu/4); per quarter and dim,
+// O_q = sum o_u 2^(m_u - M) and L_q = sum l_u 2^(m_u - M) as fused multiply-adds
+// in unit order; O = ((O_0 + O_1) + O_2) + O_3, L likewise; out = bf16(O / L).
+// The fold depends only on the row's position (its unit count).
+constexpr int kQuarters = 4;
+
+// Folds quarter q for dim d; returns (O_q, L_q).
+__device__ __forceinline__ float2 merge_quarter(const AttnDecodeArgs& a, size_t base, int nu, float M, int q, int d) {
+    const int u0 = q * nu / kQuarters, u1 = (q + 1) * nu / kQuarters;
     float O = 0.f, L = 0.f;
-    int u = 0;
-    for (; u + 8 <= nu; u += 8) {
+    int u = u0;
+    for (; u + 8 <= u1; u += 8) {
         float mv[8], lv[8], ov[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -279,12 +282,47 @@ __device__ __forceinline__ void merge128(const AttnDecodeArgs& a, int row, int h
             O = fmaf(ov[i], w, O);
         }
     }
-    for (; u < nu; ++u) {
+    for (; u < u1; ++u) {
         const float w = exp2f(a.pm[base + u] - M);
         L = fmaf(a.pl[base + u], w, L);
         O = fmaf(a.po[(base + u) * kHeadDim + d], w, O);
     }
-    a.out[(size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + d] = rn(O / L);
+    return make_float2(O, L);
+}
+
+// The merge of (row, head) by T threads (T = 256: quarters q and q+2 per thread;
+// T = 512: one quarter per thread).  Shared scratch: red (T / 32 floats), part
+// (kQuarters x 128 float2).  bar(): barrier of the T threads.
+template <int T, class Bar>
+__device__ __forceinline__ void merge(const AttnDecodeArgs& a, int row, int head, int tid, float* red, float2* part,
+                                      Bar bar) {
+    static_assert(T == 256 || T == 512, "256 or 512 threads");
+    const int d = tid & (kHeadDim - 1), q0 = tid / kHeadDim;
+    const int s = row_stream(a.rows, row);
+    const int pos = a.rows.pos0[s] + (row - a.rows.row_start[s]);
+    const int nu = pos / kUnit + 1;
+    const size_t base = ((size_t)row * a.n_q + head) * a.max_blocks;
+    float M = -INFINITY;
+    for (int u = tid; u < nu; u += T) M = fmaxf(M, a.pm[base + u]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if ((tid & 31) == 0) red[tid >> 5] = M;
+    bar();
+    M = red[0];
+#pragma unroll
+    for (int w = 1; w < T / 32; ++w) M = fmaxf(M, red[w]);
+    for (int q = q0; q < kQuarters; q += T / kHeadDim) part[q * kHeadDim + d] = merge_quarter(a, base, nu, M, q, d);
+    bar();
+    if (tid < kHeadDim) {
+        float O = part[d].x, L = part[d].y;
+#pragma unroll
+        for (int q = 1; q < kQuarters; ++q) {
+            O += part[q * kHeadDim + d].x;
+            L += part[q * kHeadDim + d].y;
+        }
+        a.out[(size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + d] = rn(O / L);
+    }
+    bar();  // the scratch may be reused
 }
 
 }  // namespace attn

@@ -184,12 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_block_kernel(const __grid_co
     attn::unit_partial<G>(a, ug, smem_u32(sm.q), sm.comb, src, [] { __syncthreads(); });
 }
 
-// One CTA of 128 threads (one per dim) per (head, row): the fold of
-// attn::merge128.
-__global__ void __launch_bounds__(kHeadDim) attn_merge_kernel(const __grid_constant__ AttnDecodeArgs a) {
+// One CTA of 512 threads (a quarter of the units per 128) per (head, row).
+__global__ void __launch_bounds__(512) attn_merge_kernel(const __grid_constant__ AttnDecodeArgs a) {
+    __shared__ float red[512 / 32];
+    __shared__ float2 part[attn::kQuarters * kHeadDim];
     pdl_wait();
     pdl_trigger();
-    attn::merge128(a, blockIdx.y, blockIdx.x, threadIdx.x);
+    attn::merge<512>(a, blockIdx.y, blockIdx.x, threadIdx.x, red, part, [] { __syncthreads(); });
 }
 
 }  // namespace
@@ -237,7 +238,7 @@ cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t c2 = {};
     c2.gridDim = dim3(a.n_q, a.rows.n_rows);
-    c2.blockDim = dim3(kHeadDim);
+    c2.blockDim = dim3(512);
     c2.stream = st;
     c2.attrs = attr;
     c2.numAttrs = pdl ? 1 : 0;

@@ -186,7 +186,7 @@ struct StepArgs {
 // grid barrier e = 1, 2, ...: [2e] arrival, [2e+1] pass.
 constexpr int kStepTsCtas = 160;
 __host__ __device__ inline int step_ts_stride(int layers) { return 2 + 2 * 6 * layers; }
-int step_smem_bytes();
+int step_smem_bytes(int rows);
 cudaError_t init_step_persistent();
 cudaError_t launch_step_persistent(const StepArgs& a, int grid, cudaStream_t st);
 

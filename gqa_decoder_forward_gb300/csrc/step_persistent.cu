@@ -28,6 +28,8 @@
 // flag that ends every other wait, and the kernel returns.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "attn_core.cuh"
 #include "common.cuh"
 #include "matvec_core.cuh"
@@ -41,9 +43,12 @@ using mvc::kConsumerWarps;
 using mvc::kKbPerStage;
 
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kDepth = 8;
+// Ring depth (stages) and activation space by rows.  (One row would leave room
+// for 11 stages; measured, 8 stream as well or better.)
+constexpr int kMaxDepth = 8;
+__host__ __device__ constexpr int ring_depth(int) { return 8; }
+__host__ __device__ constexpr int xs_bytes(int rows) { return rows * 22016 * 2; }  // down-projection lines
 constexpr int kStage = kABytes;                       // 16 KB: one weight stage or one K/V tile
-constexpr int kXsBytes = kStepMaxRows * 22016 * 2;    // activation lines / attention / merge scratch
 constexpr int kRedBytes = kConsumerWarps * 4 * 32 * 4;
 constexpr int kPhasesPerLayer = 6;
 constexpr uint32_t kSpinLimit = 1u << 24;
@@ -188,8 +193,9 @@ struct ConsumerBar {
 struct RingPos {
     int stage;
     uint32_t phase;
+    int depth;
     __device__ __forceinline__ void advance() {
-        if (++stage == kDepth) {
+        if (++stage == depth) {
             stage = 0;
             phase ^= 1u;
         }
@@ -203,7 +209,7 @@ __device__ void producer(const StepArgs& a, unsigned char* ring, uint64_t* full,
     const uint64_t pol = policy_evict_first();
     const int G = gridDim.x;
     const int nblk = attn_blocks(a), units = nblk * a.n_kv * attn_groups(a);
-    RingPos rp{0, 0u};
+    RingPos rp{0, 0u, ring_depth(a.rows.n_rows)};
     auto take = [&]() -> unsigned char* {
         if (*s_abort || !mbar_wait(&empty[rp.stage], rp.phase ^ 1u, a.status)) {
             *s_abort = 1;
@@ -272,43 +278,38 @@ struct RingSrc {
     int* status;
     volatile int* s_abort;
     int k0, p_last;
+    // the four stages of the current sub-block (set by wait)
+    int stage[4];
+    uint32_t sa[4];
     __device__ __forceinline__ RingPos at(int i) const {
         RingPos r;
-        r.stage = (base.stage + i) % kDepth;
-        r.phase = base.phase ^ (uint32_t)(((base.stage + i) / kDepth) & 1);
+        r.stage = (base.stage + i) % base.depth;
+        r.phase = base.phase ^ (uint32_t)(((base.stage + i) / base.depth) & 1);
+        r.depth = base.depth;
         return r;
     }
-    __device__ __forceinline__ uint32_t addr(int i) const { return smem_u32(ring + at(i).stage * kStage); }
     __device__ __forceinline__ static uint32_t tile(uint32_t lo, uint32_t hi, int row, int col) {
         return (col < 64 ? lo : hi) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4);
     }
-    __device__ __forceinline__ uint32_t k(int j, int row, int col) const {
-        return tile(addr(4 * j), addr(4 * j + 1), row, col);
-    }
-    __device__ __forceinline__ uint32_t v(int j, int row, int col) const {
-        return tile(addr(4 * j + 2), addr(4 * j + 3), row, col);
-    }
-    __device__ __forceinline__ void wait_stage(int i) const {
-        const RingPos r = at(i);
-        if (!*s_abort && !mbar_wait(&full[r.stage], r.phase, status)) *s_abort = 1;
-    }
-    __device__ __forceinline__ void release(int i) const {
-        __syncwarp();
-        if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[at(i).stage]);
-    }
+    __device__ __forceinline__ uint32_t k(int, int row, int col) const { return tile(sa[0], sa[1], row, col); }
+    __device__ __forceinline__ uint32_t v(int, int row, int col) const { return tile(sa[2], sa[3], row, col); }
     // this warp's key rows 16w..16w+15: values past the last visible key become
     // exact zeros (their weight is 0, and the cache there holds anything)
     __device__ __forceinline__ void wait(int j) {
-        for (int i = 0; i < 4; ++i) wait_stage(4 * j + i);
+        for (int i = 0; i < 4; ++i) {
+            const RingPos r = at(4 * j + i);
+            stage[i] = r.stage;
+            sa[i] = smem_u32(ring + r.stage * kStage);
+            if (!*s_abort && !mbar_wait(&full[r.stage], r.phase, status)) *s_abort = 1;
+        }
         const int nv = min(kPage, p_last + 1 - (k0 + j * kPage));
         const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
         const int r0 = max(nv, w * 16), r1 = w * 16 + 16;
         if (r0 < r1) {
-            const uint32_t v0 = addr(4 * j + 2), v1 = addr(4 * j + 3);
             for (int i = lane; i < (r1 - r0) * 8 * 2; i += 32) {
                 const int half = i >= (r1 - r0) * 8;
                 const int c = half ? i - (r1 - r0) * 8 : i;
-                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"((half ? v1 : v0) + r0 * 128 + c * 16),
+                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"((half ? sa[3] : sa[2]) + r0 * 128 + c * 16),
                              "r"(0u)
                              : "memory");
             }
@@ -317,8 +318,10 @@ struct RingSrc {
             __syncwarp();
         }
     }
-    __device__ __forceinline__ void done(int j) {
-        for (int i = 0; i < 4; ++i) release(4 * j + i);
+    __device__ __forceinline__ void done(int) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0)
+            for (int i = 0; i < 4; ++i) mbar_arrive(&empty[stage[i]]);
     }
 };
 
@@ -372,7 +375,7 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
     const int QD = a.n_q * kHeadDim, GQ = a.n_q / a.n_kv;
     const ConsumerBar bar;
     const uint32_t ring_u = smem_u32(ring), xs_u = smem_u32(xs);
-    RingPos rp{0, 0u};
+    RingPos rp{0, 0u, ring_depth(a.rows.n_rows)};
     unsigned epoch = 0;
     const int nblk = attn_blocks(a), units = nblk * a.n_kv * attn_groups(a);
     AttnDecodeArgs at = {};
@@ -412,7 +415,7 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
         const int tiles = phase_tiles(e), nst = (e.K + 511) / 512, kblocks = e.K / 64;
         mvc::rows_to_lines(row, norm_w, a.eps, R, e.K, xs_u, red_norm, bar);
         for (int t = blockIdx.x; t < tiles; t += G)
-            mvc::consume_tile<1>(e, t, nst, R, ring_u, kStage, kDepth, rp.stage, rp.phase, full, empty, red, s_abort,
+            mvc::consume_tile<1>(e, t, nst, R, ring_u, kStage, rp.depth, rp.stage, rp.phase, full, empty, red, s_abort,
                                  a.status, mvc::XFromLines{xs_u, R, kblocks, tig}, bar);
     };
     auto hrow = [&](int r) { return (const bf16*)a.h + (size_t)r * a.H; };
@@ -456,9 +459,13 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
                 for (int j = 0; j < 4 * x.nsub; ++j) rp.advance();
             }
         if (!grid_barrier()) return;
-        // merge: one (row, head) per 128 threads
-        for (int u = blockIdx.x * 2 + (tid >> 7); u < R * a.n_q; u += 2 * G)
-            attn::merge128(at, u / a.n_q, u % a.n_q, tid & (kHeadDim - 1));
+        // merge: one (row, head) at a time
+        {
+            float* redm = reinterpret_cast<float*>(xs);
+            float2* part = reinterpret_cast<float2*>(xs + 64);
+            for (int u = blockIdx.x; u < R * a.n_q; u += G)
+                attn::merge<kConsumerWarps * 32>(at, u / a.n_q, u % a.n_q, tid, redm, part, bar);
+        }
         if (!grid_barrier()) return;
         matvec(l, PH_O, aorow, nullptr);
         if (!grid_barrier()) return;
@@ -476,15 +483,16 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     extern __shared__ unsigned char smem_raw[];
     unsigned char* ring =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned char* xs = ring + kDepth * kStage;
-    float* red = reinterpret_cast<float*>(xs + kXsBytes);
+    const int depth = ring_depth(a.rows.n_rows);
+    unsigned char* xs = ring + depth * kStage;
+    float* red = reinterpret_cast<float*>(xs + xs_bytes(a.rows.n_rows));
     float* red_norm = red + kRedBytes / 4;
     uint64_t* full = reinterpret_cast<uint64_t*>(red_norm + 8 * kStepMaxRows);
-    uint64_t* empty = full + kDepth;
-    volatile int* s_abort = reinterpret_cast<volatile int*>(empty + kDepth);
+    uint64_t* empty = full + kMaxDepth;
+    volatile int* s_abort = reinterpret_cast<volatile int*>(empty + kMaxDepth);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kDepth; ++s) {
+        for (int s = 0; s < depth; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
@@ -505,12 +513,13 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
 
 }  // namespace
 
-int step_smem_bytes() {
-    return 1024 + kDepth * kStage + kXsBytes + kRedBytes + 8 * kStepMaxRows * 4 + 2 * kDepth * 8 + 64;
+int step_smem_bytes(int rows) {
+    return 1024 + ring_depth(rows) * kStage + xs_bytes(rows) + kRedBytes + 8 * kStepMaxRows * 4 + 2 * kMaxDepth * 8 + 64;
 }
 
 cudaError_t init_step_persistent() {
-    return cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, step_smem_bytes());
+    return cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                std::max(step_smem_bytes(1), step_smem_bytes(2)));
 }
 
 cudaError_t launch_step_persistent(const StepArgs& a, int grid, cudaStream_t st) {
@@ -525,7 +534,7 @@ cudaError_t launch_step_persistent(const StepArgs& a, int grid, cudaStream_t st)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = step_smem_bytes();
+    cfg.dynamicSmemBytes = step_smem_bytes(a.rows.n_rows);
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
