@@ -64,6 +64,9 @@ def lib():
         L.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
         L.orc_get_threads.restype = ctypes.c_int
         L.orc_argmax.restype = ctypes.c_int
+        L.orc_sample.restype = ctypes.c_int
+        L.orc_sample.argtypes = [_u16p, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_double,
+                                 ctypes.POINTER(ctypes.c_double), _i32p]
         L.orc_forward.restype = ctypes.c_int
         _lib = L
     return _lib
@@ -186,6 +189,18 @@ def argmax(logits):
     rows = logits.size // V
     ids = np.empty(rows, np.int32)
     st = lib().orc_argmax(_p(logits, _u16p), rows, V, _p(ids, _i32p))
+    return ids, int(st)
+
+
+def sample(logits, temperature: float, top_k: int, top_p: float, u):
+    """Seeded draw per row (see orc_sample): returns (ids int32 [rows], status)."""
+    logits = _u16(logits)
+    V = logits.shape[-1]
+    rows = logits.size // V
+    uu = np.ascontiguousarray(np.asarray(u, np.float64).reshape(rows))
+    ids = np.empty(rows, np.int32)
+    st = lib().orc_sample(_p(logits, _u16p), rows, V, float(temperature), int(top_k), float(top_p),
+                          uu.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), _p(ids, _i32p))
     return ids, int(st)
 
 

@@ -264,6 +264,82 @@ int orc_argmax(const uint16_t* logits, int rows, int V, int32_t* ids) {
     return status;
 }
 
+// Seeded sampling of one token per row (the GPU draw the pages name beside
+// argmax: "argmax or tf_sample_full"; temperature, top-k and top-p as in the
+// release's recommended settings).  The pages fix no algorithm; the reading
+// (also listed in the design doc), over a row's bf16 logits z with T > 0, k >= 0,
+// 0 < p, and a uniform u in [0, 1) given by the caller:
+//   1. candidates C: all ids if k == 0 or k >= V, else the ids whose logit is at
+//      least the k-th largest logit (counted with multiplicity; ties included);
+//   2. weight of a logit value v: w(v) = exp((v - z_max) / T) in double;
+//      mass of a value: (number of candidates holding it) * w(v);
+//   3. nucleus N: walking the distinct candidate values from the largest down
+//      and accumulating their mass, the first value at which the running mass
+//      reaches p * (mass of C) is the cut; N = candidates with logit >= the cut
+//      (all of C when p >= 1); W = the running mass at the cut;
+//   4. draw: the smallest id j in N whose running sum of w over N in id order
+//      exceeds u * W (the largest id of N if rounding leaves none).
+// A row holding NaN or +-Inf gets -1 and the status -1.
+int orc_sample(const uint16_t* logits, int rows, int V, double temperature, int top_k, double top_p,
+               const double* u, int32_t* ids) {
+    int status = 0;
+    for (int r = 0; r < rows; ++r) {
+        const uint16_t* lr = logits + (long)r * V;
+        std::vector<double> z(V);
+        bool finite = true;
+        for (int i = 0; i < V; ++i) {
+            z[i] = bf16_val(lr[i]);
+            if (!std::isfinite(z[i])) finite = false;
+        }
+        if (!finite) {
+            ids[r] = -1;
+            status = -1;
+            continue;
+        }
+        std::vector<double> sorted(z);
+        std::sort(sorted.begin(), sorted.end(), std::greater<double>());
+        const double z_max = sorted[0];
+        const double kth = (top_k > 0 && top_k < V) ? sorted[top_k - 1] : sorted[V - 1];
+        // distinct candidate values, largest first, with their counts
+        std::vector<std::pair<double, long>> vals;
+        for (double v : sorted) {
+            if (v < kth) break;
+            if (vals.empty() || vals.back().first != v) vals.push_back({v, 0});
+            vals.back().second += 1;
+        }
+        auto w = [&](double v) { return std::exp((v - z_max) / temperature); };
+        double total = 0.0;
+        for (auto& vc : vals) total += (double)vc.second * w(vc.first);
+        double cut = kth, mass = total;
+        if (top_p < 1.0) {
+            const double goal = top_p * total;
+            double run = 0.0;
+            for (auto& vc : vals) {
+                run += (double)vc.second * w(vc.first);
+                if (run >= goal) {
+                    cut = vc.first;
+                    mass = run;
+                    break;
+                }
+            }
+        }
+        const double target = u[r] * mass;
+        double run = 0.0;
+        int pick = -1, last = -1;
+        for (int i = 0; i < V; ++i) {
+            if (z[i] < cut) continue;
+            last = i;
+            run += w(z[i]);
+            if (run > target) {
+                pick = i;
+                break;
+            }
+        }
+        ids[r] = pick >= 0 ? pick : last;
+    }
+    return status;
+}
+
 // ---- the model --------------------------------------------------------------
 
 struct orc_config {
