@@ -533,6 +533,24 @@ def run_op(args):
     w["lm_head"] = torch.zeros(64, dtype=torch.bfloat16, device=dev)
     R, ctx = args.rows, args.context
     m = tfl.Model(one, w, max_rows=max(64, R), max_decode_rows=64, max_context=ctx + R)
+    if args.op == "sample":
+        # seeded draw at temperature 0.6, top-k 20, top-p 0.95 over the 166,912-id vocabulary
+        lg = synth.normal_bf16(5, 5, (R, one.vocab), 2.0, dev)
+        u = torch.rand(R, generator=torch.Generator().manual_seed(7)).to(dev)
+        ids = torch.empty(R, dtype=torch.int32, device=dev)
+        for _ in range(args.warmup):
+            m.sample(lg, 0.6, 20, 0.95, u, ids)
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(st)
+        for _ in range(args.steps):
+            m.sample(lg, 0.6, 20, 0.95, u, ids)
+        t1.record(st)
+        torch.cuda.synchronize()
+        print(json.dumps({"op": "sample", "rows": R, "vocab": one.vocab, "us_per_launch":
+                          round(t0.elapsed_time(t1) / args.steps * 1e3, 2), "status": m.status()}), flush=True)
+        return
     kv = m.kv(ctx + R)
     K, V = synth.kv_contents(one, 22, 0, ctx + R, dev)
     kv.write(0, 0, K, V)

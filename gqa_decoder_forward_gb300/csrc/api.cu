@@ -91,7 +91,7 @@ int qualify(const tfl_config* c) {
 
 // Workspace layout (byte offsets, 256-byte aligned regions).
 struct Layout {
-    size_t h, xn, q, ao, act, pm, pl, po, cos_t, sin_t, status, wmaps, norms, sync, zero, ts, total;
+    size_t h, xn, q, ao, act, pm, pl, po, cos_t, sin_t, status, wmaps, norms, sync, zero, ts, scounts, swtab, total;
     int max_blocks;
 };
 
@@ -126,6 +126,9 @@ Layout layout(const tfl_config* c) {
     L.sync = take(256);
     L.zero = take((size_t)c->hidden * 2);
     L.ts = take((size_t)kStepTsCtas * step_ts_stride(c->layers) * 8);
+    // sampling scratch: a count and a weight per bf16 value, per row
+    L.scounts = take(dr * 65536 * 4);
+    L.swtab = take(dr * 65536 * 8);
     L.total = off;
     return L;
 }
@@ -228,13 +231,14 @@ constexpr int kMaxFusedNormRows = 8;
 // Kernel families timed by tfl_profile (names in tfl_profile_kind).
 enum Kind {
     K_EMBED, K_NORM, K_QKV, K_ATTN, K_MERGE, K_O, K_GATEUP, K_DOWN, K_LMHEAD, K_ARGMAX,
-    K_GQKV, K_GO, K_GGATEUP, K_GDOWN, K_PATTN, K_STEP, K_COUNT
+    K_GQKV, K_GO, K_GGATEUP, K_GDOWN, K_PATTN, K_STEP, K_SAMPLE, K_COUNT
 };
 const char* const kKindName[K_COUNT] = {"embed_rmsnorm", "rmsnorm", "matvec_qkv_rope", "attn_decode_block",
                                         "attn_decode_merge", "matvec_o_residual", "matvec_gate_up_swiglu",
                                         "matvec_down_residual", "matvec_lm_head", "argmax",
                                         "gemm_qkv_rope", "gemm_o_residual", "gemm_gate_up_swiglu",
-                                        "gemm_down_residual", "attn_prefill", "decode_step_persistent"};
+                                        "gemm_down_residual", "attn_prefill", "decode_step_persistent",
+                                        "sample"};
 
 struct Mark {
     int kind;
@@ -255,6 +259,8 @@ struct tfl_model {
     unsigned* sync;
     bf16* zero_row;
     unsigned long long* ts;  // decode-step phase stamps (written while profiling)
+    unsigned* scounts;       // sampling scratch
+    double* swtab;
     bool ts_valid = false;
     bool persistent = true; // decode steps of <= kStepMaxRows rows as one launch
     bool pdl;
@@ -818,6 +824,8 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
     m->sync = (unsigned*)(m->ws + L.sync);
     m->zero_row = (bf16*)(m->ws + L.zero);
     m->ts = (unsigned long long*)(m->ws + L.ts);
+    m->scounts = (unsigned*)(m->ws + L.scounts);
+    m->swtab = (double*)(m->ws + L.swtab);
     m->pdl = true;
 
     // projections: TMA descriptors of every weight matrix and activation buffer
@@ -1025,6 +1033,24 @@ int tfl_head(tfl_model* m, const void* h, int rows, void* logits, void* stream) 
     CK(cudaMemcpyAsync(m->h, h, (size_t)rows * m->cfg.hidden * 2, cudaMemcpyDeviceToDevice, st));
     int e = run_head(m, 0, rows, logits, m->cfg.vocab, st);
     return e ? e : ok();
+}
+
+int tfl_sample(tfl_model* m, const void* logits, int n_rows, float temperature, int top_k, float top_p,
+               const float* u, int32_t* ids, void* stream) {
+    if (!m || !logits || !u || !ids) return fail(TFL_E_ARG, "NULL model, logits, u or ids");
+    if (n_rows < 1 || n_rows > m->cfg.max_decode_rows)
+        return fail(TFL_E_ARG, "n_rows %d outside 1..max_decode_rows %d", n_rows, m->cfg.max_decode_rows);
+    if (!(temperature > 0.f) || !std::isfinite(temperature))
+        return fail(TFL_E_ARG, "temperature %g must be finite and > 0 (use tfl_argmax for greedy)", (double)temperature);
+    if (top_k < 0) return fail(TFL_E_ARG, "top_k %d < 0", top_k);
+    if (!(top_p > 0.f) || std::isnan(top_p)) return fail(TFL_E_ARG, "top_p %g must be > 0", (double)top_p);
+    if (((uintptr_t)logits & 1u) || ((uintptr_t)u & 3u) || ((uintptr_t)ids & 3u))
+        return fail(TFL_E_ARG, "misaligned logits, u or ids");
+    cudaStream_t st = (cudaStream_t)stream;
+    LAUNCH(m, K_SAMPLE, st,
+           launch_sample((const bf16*)logits, n_rows, m->cfg.vocab, temperature, top_k, top_p, u, ids, m->status,
+                         m->scounts, m->swtab, st, m->pdl && st != nullptr));
+    return ok();
 }
 
 int tfl_argmax(tfl_model* m, const void* logits, int n_rows, int32_t* ids, void* stream) {

@@ -190,6 +190,11 @@ int step_smem_bytes(int rows);
 cudaError_t init_step_persistent();
 cudaError_t launch_step_persistent(const StepArgs& a, int grid, cudaStream_t st);
 
+// Seeded sampling (sample.cu); counts / wtab: per row 65,536 unsigned / double of scratch.
+cudaError_t launch_sample(const bf16* logits, int n_rows, int V, float temperature, int top_k, float top_p,
+                          const float* u, int32_t* ids, int* status, unsigned* counts, double* wtab, cudaStream_t st,
+                          bool pdl);
+
 cudaError_t launch_argmax(const bf16* logits, int n_rows, int V, int32_t* ids, int* status, cudaStream_t st,
                           bool pdl);
 

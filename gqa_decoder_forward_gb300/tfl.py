@@ -78,6 +78,8 @@ SIGNATURES = {
     "tfl_attention_decode_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp]),
     "tfl_profile": (ctypes.c_int, [_vp, ctypes.c_int]),
     "tfl_set_persistent": (ctypes.c_int, [_vp, ctypes.c_int]),
+    "tfl_sample": (ctypes.c_int, [_vp, _vp, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_float, _vp, _vp,
+                                  _vp]),
     "tfl_step_phases": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_double), ctypes.c_int]),
     "tfl_profile_read": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_long)]),
@@ -207,6 +209,13 @@ class Model:
 
     def argmax(self, logits: torch.Tensor, ids: torch.Tensor, stream=None):
         return tfl_argmax(self, logits, ids, stream)
+
+    def sample(self, logits: torch.Tensor, temperature: float, top_k: int, top_p: float, u: torch.Tensor,
+               ids: torch.Tensor, stream=None):
+        """Seeded draw per row (u: float32 CUDA tensor of uniforms in [0, 1))."""
+        assert u.dtype == torch.float32 and u.is_cuda and ids.dtype == torch.int32
+        return _check(lib().tfl_sample(self.handle, _ptr(logits), logits.shape[0], float(temperature), int(top_k),
+                                       float(top_p), _ptr(u), _ptr(ids), _stream(stream)))
 
     def status(self, stream=None) -> int:
         return lib().tfl_status(self.handle, _stream(stream))

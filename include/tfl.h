@@ -223,6 +223,24 @@ int tfl_prefill_chunk(tfl_model* model, tfl_kv* kv, const int32_t* ids, int n_ro
 int tfl_argmax(tfl_model* model, const void* logits, int n_rows, int32_t* ids, void* stream);
 
 /*
+ * Sampled ids (device int32 [n_rows], n_rows 1..max_decode_rows) from logits
+ * (device bf16 [n_rows][V]) with temperature T > 0, top_k (0 = no cut) and
+ * top_p (>= 1 = no cut); u: device float [n_rows], the caller's uniform draws in
+ * [0, 1) (its seeded random numbers).  Per row: candidates = ids whose logit is
+ * at least the top_k-th largest (ties included); weights exp((z - z_max)/T) in
+ * double; nucleus = candidates at or above the first value (largest down) at
+ * which the running mass of the values reaches top_p of the candidates' mass;
+ * result = the smallest nucleus id whose running weight in id order exceeds
+ * u x (nucleus mass).  The pages name a seeded GPU draw with temperature and
+ * top-p beside argmax but fix no algorithm; this is the reading taken.  A row
+ * holding NaN or +-Inf gets -1 and raises the device status word (tfl_status:
+ * TFL_E_NONFINITE).  Deterministic.  Uses the model's workspace (serialise
+ * calls on one model).
+ */
+int tfl_sample(tfl_model* model, const void* logits, int n_rows, float temperature, int top_k, float top_p,
+               const float* u, int32_t* ids, void* stream);
+
+/*
  * Synchronises `stream`, reads and clears the device status word: returns
  * TFL_OK, TFL_E_NONFINITE (an argmax saw a non-finite logit) or TFL_E_DEVICE
  * (a kernel gave up a bounded wait), or TFL_E_CUDA if the stream had failed.
