@@ -717,6 +717,28 @@ int kv_handle_view(const tfl_kv* kv, KvView* out, int* max_pos, int* n_q, int* n
 
 void set_last_error(const char* msg) { g_err = msg; }
 
+int api_fail(int code, const char* msg) { return fail(code, "%s", msg); }
+
+int kv_prefix_geometry(const tfl_kv* kv, const tfl_model* m, bf16** pages, int* n_pages, int* length, int* max_pos) {
+    if (!kv || kv->model != m) return TFL_E_ARG;
+    *pages = kv->pages;
+    *n_pages = kv->n_pages;
+    *length = kv->length;
+    *max_pos = kv->max_pos;
+    return TFL_OK;
+}
+
+int kv_set_length(tfl_kv* kv, int length) {
+    kv->length = length;
+    return TFL_OK;
+}
+
+int model_geometry(const tfl_model* m, int* layers, int* n_kv) {
+    *layers = m->cfg.layers;
+    *n_kv = m->cfg.n_kv;
+    return TFL_OK;
+}
+
 }  // namespace tfl
 
 // ---- C ABI ------------------------------------------------------------------------

@@ -14,6 +14,7 @@ import ctypes
 import os
 from typing import Sequence
 
+import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -78,6 +79,14 @@ SIGNATURES = {
     "tfl_attention_decode_noalloc": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp]),
     "tfl_profile": (ctypes.c_int, [_vp, ctypes.c_int]),
     "tfl_set_persistent": (ctypes.c_int, [_vp, ctypes.c_int]),
+    "tfl_kv_copy_prefix": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, _vp]),
+    "tfl_prefix_store_new": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(_vp)]),
+    "tfl_prefix_store_free": (None, [_vp]),
+    "tfl_prefix_store_put": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32), ctypes.c_int, _vp]),
+    "tfl_prefix_store_match": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int32), ctypes.c_int,
+                                              ctypes.POINTER(_vp), ctypes.POINTER(ctypes.c_int)]),
+    "tfl_prefix_store_remove": (ctypes.c_int, [_vp, _vp]),
+    "tfl_prefix_store_size": (ctypes.c_int, [_vp]),
     "tfl_sample": (ctypes.c_int, [_vp, _vp, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_float, _vp, _vp,
                                   _vp]),
     "tfl_step_phases": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_double), ctypes.c_int]),
@@ -319,6 +328,51 @@ def tfl_attention_decode_noalloc(kv: "KV", layer: int, pos0: int, q: torch.Tenso
 
 def tfl_profile(model: Model, enable: bool):
     return _check(lib().tfl_profile(model.handle, 1 if enable else 0))
+
+
+def tfl_kv_copy_prefix(model: Model, src: "KV", dst: "KV", n: int, stream=None):
+    """Copies positions [0, n) of every layer from src to dst; length(dst) = n."""
+    _check(lib().tfl_kv_copy_prefix(model.handle, src.handle, dst.handle, n, _stream(stream)))
+
+
+class PrefixStore:
+    """Host index of caches holding prompt prefixes (tfl_prefix_store_*); the
+    caches stay owned by the caller (KV objects are kept referenced here)."""
+
+    def __init__(self, max_entries: int):
+        h = _vp()
+        _check(lib().tfl_prefix_store_new(max_entries, ctypes.byref(h)))
+        self.handle = h
+        self._kvs = {}
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            lib().tfl_prefix_store_free(self.handle)
+            self.handle = None
+
+    @staticmethod
+    def _tok(tokens):
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        return t, t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+    def put(self, tokens, kv: "KV"):
+        t, p = self._tok(tokens)
+        _check(lib().tfl_prefix_store_put(self.handle, p, len(t), kv.handle))
+        self._kvs[kv.handle.value if hasattr(kv.handle, "value") else kv.handle] = kv
+
+    def match(self, tokens):
+        """(KV or None, matched token count)."""
+        t, p = self._tok(tokens)
+        h, n = _vp(), ctypes.c_int()
+        _check(lib().tfl_prefix_store_match(self.handle, p, len(t), ctypes.byref(h), ctypes.byref(n)))
+        return (self._kvs.get(h.value) if h.value else None), n.value
+
+    def remove(self, kv: "KV"):
+        _check(lib().tfl_prefix_store_remove(self.handle, kv.handle))
+        self._kvs.pop(kv.handle.value if hasattr(kv.handle, "value") else kv.handle, None)
+
+    def __len__(self):
+        return lib().tfl_prefix_store_size(self.handle)
 
 
 STEP_PHASES = ("qkv", "attention", "merge", "o", "gate_up", "down", "barrier", "head", "total")

@@ -176,6 +176,38 @@ int tfl_kv_write(tfl_model* model, tfl_kv* kv, int layer, int pos0, int n, const
 int tfl_kv_read(tfl_model* model, const tfl_kv* kv, int layer, int pos0, int n, void* k, void* v,
                 void* stream);
 
+/* ---- prompt cache ------------------------------------------------------------ */
+
+/*
+ * Copies the keys and values of positions [0, n) of every layer from src to
+ * dst (both of this model; n <= length(src), n <= capacity(dst)) and sets
+ * length(dst) = n.  Prefilling the rest of a prompt into dst then gives the
+ * same bits as prefilling the whole prompt fresh (a prompt resumed from a kept
+ * prefix, pull request #1415: "resumed prompts equal to fresh ones").  One
+ * 2-D device copy of the whole pages involved, enqueued on stream; src and dst
+ * must not be written by other work meanwhile.
+ */
+int tfl_kv_copy_prefix(tfl_model* model, const tfl_kv* src, tfl_kv* dst, int n, void* stream);
+
+/*
+ * A host-side index of caches that hold prompt prefixes (the prompt cache of
+ * the pages' served setup).  The caller owns the caches; the store keeps a copy
+ * of each entry's tokens and a pointer to its cache, and never touches the
+ * cache itself.  put registers `kv` under tokens[0, n) (host int32, n >= 1; the
+ * caller keeps length(kv) >= n while the entry exists); TFL_E_CAPACITY when the
+ * store holds max_entries entries.  match returns the entry with the longest
+ * common token prefix with tokens[0, n) and that length (ties: the entry put
+ * last; none: *kv = NULL, *matched = 0).  remove drops the entries of kv.
+ * No counterpart API on the pages (they describe the behaviour, not an API).
+ */
+typedef struct tfl_prefix_store tfl_prefix_store;
+int tfl_prefix_store_new(int max_entries, tfl_prefix_store** out);
+void tfl_prefix_store_free(tfl_prefix_store* store);
+int tfl_prefix_store_put(tfl_prefix_store* store, const int32_t* tokens, int n, tfl_kv* kv);
+int tfl_prefix_store_match(tfl_prefix_store* store, const int32_t* tokens, int n, tfl_kv** kv, int* matched);
+int tfl_prefix_store_remove(tfl_prefix_store* store, const tfl_kv* kv);
+int tfl_prefix_store_size(const tfl_prefix_store* store);
+
 /* ---- forward ------------------------------------------------------------------ */
 
 /*

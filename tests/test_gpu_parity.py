@@ -531,3 +531,38 @@ def test_fused_norm_ops_equal_norm_then_projection(tiny, R):
     lg = torch.empty_like(l_ref)
     tfl.tfl_layer_op(m, "norm_lm_head", 0, h, lg)
     assert torch.equal(lg.view(torch.int16), l_ref.view(torch.int16))
+
+
+# ---- prompt cache ---------------------------------------------------------------------
+
+def test_resume_from_prefix_store_equals_fresh(tiny):
+    """A prompt whose first 250 tokens sit in a stored cache: copy the prefix,
+    prefill the rest, then decode; every logit equals the prompt prefilled fresh."""
+    w, _ = tiny
+    m = _tiny_model(w, max_rows=512, max_context=512)
+    first = synth.uniform_ids(91, 300, TINY.vocab, "cuda")
+    second = torch.cat([first[:250], synth.uniform_ids(92, 60, TINY.vocab, "cuda")]).contiguous()
+    stored = m.kv(320)
+    m.prefill_chunk(stored, first)
+    store = tfl.PrefixStore(4)
+    store.put(first.cpu().numpy(), stored)
+    src, n = store.match(second.cpu().numpy())
+    assert src is stored and n == 250
+    resumed = m.kv(320)
+    tfl.tfl_kv_copy_prefix(m, src, resumed, n)
+    assert resumed.length == 250
+    lr = torch.empty((60, TINY.vocab), dtype=torch.bfloat16, device="cuda")
+    m.prefill_chunk(resumed, second[250:].contiguous(), lr, all_rows=True)
+    fresh = m.kv(320)
+    lf = torch.empty((310, TINY.vocab), dtype=torch.bfloat16, device="cuda")
+    m.prefill_chunk(fresh, second, lf, all_rows=True)
+    assert torch.equal(lr.view(torch.int16), lf[250:].view(torch.int16))
+    feed = synth.uniform_ids(93, 4, TINY.vocab, "cuda")
+    for t in range(4):
+        a = torch.empty((1, TINY.vocab), dtype=torch.bfloat16, device="cuda")
+        b = torch.empty_like(a)
+        m.decode_step([resumed], feed[t:t + 1].contiguous(), [1], a)
+        m.decode_step([fresh], feed[t:t + 1].contiguous(), [1], b)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), t
+    with pytest.raises(tfl.TflError):
+        tfl.tfl_kv_copy_prefix(m, stored, resumed, 301)   # beyond length(src)
