@@ -54,6 +54,8 @@ def parse():
                         "positions) instead of the default line")
     p.add_argument("--prompt", action="store_true",
                    help="--op runs the prompt-chunk kernel of the op (rows up to 2,048)")
+    p.add_argument("--drafted-tokens", type=int, default=64,
+                   help="greedy tokens for the drafted-decode figures of the default line (0 = skip them)")
     return p.parse_args()
 
 
@@ -293,6 +295,7 @@ def run_tfl(args, world, rank, local):
     shape = SHAPE.with_layers(args.layers)
     ctx = args.context
     extra = args.warmup + args.steps + 16 + 16 + 18 + 8  # warm-up, timed, profiled, e2e, per-launch steps
+    extra = max(extra, args.drafted_tokens + 1)        # the drafted-decode caches hold prompt + reply
     max_ctx = ctx + extra
     dev = torch.device("cuda", torch.cuda.current_device())
 
@@ -317,6 +320,7 @@ def run_tfl(args, world, rank, local):
         torch.cuda.synchronize()
         prefill_s = e0.elapsed_time(e1) / 1e3
         model.argmax(logits, nxt)
+        first_id = int(nxt.item())
         # the same prefill once more on a second cache, every launch bracketed by events
         kv2 = model.kv(max_ctx)
         lg2 = torch.empty_like(logits)
@@ -423,6 +427,10 @@ def run_tfl(args, world, rank, local):
                 "frac": round(ach / peak, 4), "traffic": ncu_traffic(dom_name), "peak_kind": peak_kind,
                 "bytes_per_launch": dom_bytes, "us_per_launch": round(dom_ms / dom_n * 1e3, 2)}
 
+    drafted = None
+    if args.kv == "prefill" and args.drafted_tokens > 0:
+        drafted = drafted_figures(model, kv, ids, first_id, ctx, args.drafted_tokens, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         per_tok, cores, desc, _, _ = oracle_sample(ctx, min_seconds=10.0)
@@ -456,10 +464,71 @@ def run_tfl(args, world, rank, local):
                 "d2h_bytes_per_step": 4},
         "clocks": clk.summary(),
         "status": status,
+        "drafted": drafted,
         "cpu_baseline": cpu,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+DRAFTER_LAYERS = 4
+
+
+def drafted_figures(model, kv, ids, first_id, ctx, n, dev):
+    """Drafted greedy decode of n tokens after the prompt (tfl_decode_drafted),
+    with copy drafts and with a smaller random-init drafter of the same vocabulary
+    (the 33B width, DRAFTER_LAYERS layers: about the bytes per step of a 3B
+    model), against n plain one-row steps from the same prompt cache.  Wall-clock
+    seconds around each host-synchronous call."""
+    from gqa_decoder_forward_gb300 import tfl
+    shape = model.shape
+    prompt = [int(x) for x in ids.cpu()]
+    context = prompt + [first_id]
+    cap = ctx + n + 1
+
+    def cache_from_prompt():
+        c = model.kv(cap)
+        tfl.tfl_kv_copy_prefix(model, kv, c, ctx)
+        return c
+
+    V = shape.vocab
+    kvp = cache_from_prompt()
+    pin = torch.tensor([first_id], dtype=torch.int32, device=dev)
+    lg = torch.empty((1, V), dtype=torch.bfloat16, device=dev)
+    out = torch.empty(n, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    w0 = time.perf_counter()
+    for t in range(n):
+        model.decode_step([kvp], pin if t == 0 else out[t - 1:t], [1], lg)
+        model.argmax(lg, out[t:t + 1])
+    ref = out.cpu().numpy()
+    plain_s = time.perf_counter() - w0
+    del kvp
+    res = {"tokens": n, "plain_tok_s": round(n / plain_s, 2),
+           "reply_distinct_ids": int(len(set(ref.tolist())))}
+
+    dshape = shape.with_layers(DRAFTER_LAYERS)
+    dw = synth.model_weights(dshape, 23, dev)
+    drafter = tfl.Model(dshape, dw, max_rows=2048, max_decode_rows=16, max_context=cap)
+    for name, k, use in (("copy", 7, False), ("drafter", 3, True)):
+        c = cache_from_prompt()
+        d = dkv = None
+        if use:
+            d, dkv = drafter, drafter.kv(cap)
+            for s0 in range(0, ctx, 2048):
+                drafter.prefill_chunk(dkv, ids[s0:s0 + 2048].contiguous())
+        torch.cuda.synchronize()
+        w0 = time.perf_counter()
+        got, st = model.decode_drafted(c, context, n, k, d, dkv)
+        secs = time.perf_counter() - w0
+        res[name] = {"draft_len": k, "tok_s": round(n / secs, 2), "equal_plain": bool((got == ref).all()),
+                     "accept_rate": round(st["accepted"] / max(1, st["drafted"]), 4), **st}
+        if use:
+            res[name]["drafter"] = f"{DRAFTER_LAYERS}-layer 33B-width random-init model, seed 23"
+        del c, dkv
+    del drafter, dw
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_concurrent(args):

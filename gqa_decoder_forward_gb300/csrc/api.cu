@@ -739,6 +739,18 @@ int model_geometry(const tfl_model* m, int* layers, int* n_kv) {
     return TFL_OK;
 }
 
+const tfl_config* model_config(const tfl_model* m) { return m ? &m->cfg : nullptr; }
+
+tfl_model* kv_owner(const tfl_kv* kv) { return kv ? kv->model : nullptr; }
+
+// Greedy ids of draft rows: a non-finite row proposes id 0 (the served model's
+// check then decides) and raises the drafter's non-finite status bit.
+int draft_argmax(tfl_model* m, const void* logits, int n_rows, int32_t* ids, cudaStream_t st) {
+    LAUNCH(m, K_ARGMAX, st, launch_argmax((const bf16*)logits, n_rows, m->cfg.vocab, ids, m->status, st,
+                                          m->pdl && st != nullptr, 0));
+    return TFL_OK;
+}
+
 }  // namespace tfl
 
 // ---- C ABI ------------------------------------------------------------------------

@@ -195,8 +195,11 @@ cudaError_t launch_sample(const bf16* logits, int n_rows, int V, float temperatu
                           const float* u, int32_t* ids, int* status, unsigned* counts, double* wtab, cudaStream_t st,
                           bool pdl);
 
+// Greedy id per row (ties to the lower id); a row holding NaN / +-Inf gets
+// bad_id (-1 for callers, 0 for a draft, which the served model then checks)
+// and raises kStatusNonFinite.
 cudaError_t launch_argmax(const bf16* logits, int n_rows, int V, int32_t* ids, int* status, cudaStream_t st,
-                          bool pdl);
+                          bool pdl, int bad_id = -1);
 
 cudaError_t launch_kv_copy(bf16* cache_pages, const int* table, int n_pages, int n_kv, int layer, int pos0, int n,
                            bf16* k, bf16* v, bool to_cache, cudaStream_t st);

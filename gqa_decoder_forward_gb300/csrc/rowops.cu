@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const int32
 
 constexpr int kArgThreads = 1024;
 
-__global__ void __launch_bounds__(kArgThreads) argmax_kernel(const bf16* logits, int V, int32_t* ids, int* status) {
+__global__ void __launch_bounds__(kArgThreads) argmax_kernel(const bf16* logits, int V, int32_t* ids, int* status,
+                                                              int bad_id) {
     __shared__ float bv[kArgThreads / 32];
     __shared__ int bi[kArgThreads / 32];
     __shared__ int bad_any;
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kArgThreads) argmax_kernel(const bf16* logits,
         for (int w = 1; w < kArgThreads / 32; ++w)
             if (bv[w] > b || (bv[w] == b && bi[w] < j)) { b = bv[w]; j = bi[w]; }
         if (bad_any) {
-            ids[blockIdx.x] = -1;
+            ids[blockIdx.x] = bad_id;
             atomicOr(status, kStatusNonFinite);
         } else {
             ids[blockIdx.x] = j;
@@ -163,11 +164,11 @@ cudaError_t launch_embed_rmsnorm(const int32_t* ids, const bf16* embed, int voca
 }
 
 cudaError_t launch_argmax(const bf16* logits, int n_rows, int V, int32_t* ids, int* status, cudaStream_t st,
-                          bool pdl) {
+                          bool pdl, int bad_id) {
     if (V % 8 != 0 || n_rows < 1) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t c = row_cfg(n_rows, kArgThreads, st, attr, pdl);
-    return cudaLaunchKernelEx(&c, argmax_kernel, logits, V, ids, status);
+    return cudaLaunchKernelEx(&c, argmax_kernel, logits, V, ids, status, bad_id);
 }
 
 cudaError_t launch_kv_copy(bf16* pages, const int* table, int n_pages, int n_kv, int layer, int pos0, int n, bf16* k,

@@ -41,6 +41,11 @@ class tfl_config(ctypes.Structure):
                 ("max_rows", ctypes.c_int), ("max_decode_rows", ctypes.c_int), ("max_context", ctypes.c_int)]
 
 
+class tfl_draft_stats(ctypes.Structure):
+    _fields_ = [("rounds", ctypes.c_longlong), ("drafted", ctypes.c_longlong), ("accepted", ctypes.c_longlong),
+                ("target_rows", ctypes.c_longlong), ("drafter_rows", ctypes.c_longlong)]
+
+
 class tfl_weights(ctypes.Structure):
     _fields_ = [("embed", _vp), ("final_norm", _vp), ("lm_head", _vp)] + [
         (n, ctypes.POINTER(_vp)) for n in
@@ -90,6 +95,12 @@ SIGNATURES = {
     "tfl_sample": (ctypes.c_int, [_vp, _vp, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_float, _vp, _vp,
                                   _vp]),
     "tfl_step_phases": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_double), ctypes.c_int]),
+    "tfl_drafted_workspace_bytes": (ctypes.c_size_t, [_vp, ctypes.c_int]),
+    "tfl_decode_drafted": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                                          ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int32), _vp,
+                                          ctypes.c_size_t, _vp, _vp]),
+    "tfl_copy_draft": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), ctypes.c_int, ctypes.c_int,
+                                      ctypes.POINTER(ctypes.c_int32)]),
     "tfl_profile_read": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_long)]),
     "tfl_profile_kind": (ctypes.c_char_p, [ctypes.c_int]),
@@ -228,6 +239,13 @@ class Model:
 
     def status(self, stream=None) -> int:
         return lib().tfl_status(self.handle, _stream(stream))
+
+    def decode_drafted(self, kv: "KV", context, n_tokens: int, draft_len: int, drafter: "Model" = None,
+                       dkv: "KV" = None, stream=None):
+        """Drafted greedy decode (tfl_decode_drafted): context = the tokens so far
+        (host ints, the last one pending, length(kv) == len(context) - 1).
+        Returns (numpy int32 [n_tokens] greedy ids, stats dict)."""
+        return tfl_decode_drafted(self, kv, context, n_tokens, draft_len, drafter, dkv, stream)
 
 
 class KV:
@@ -373,6 +391,41 @@ class PrefixStore:
 
     def __len__(self):
         return lib().tfl_prefix_store_size(self.handle)
+
+
+def tfl_copy_draft(tokens, max_draft: int) -> np.ndarray:
+    """Copy-draft guesses for the tokens so far (host only)."""
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    out = np.zeros(max(max_draft, 1), np.int32)
+    n = _check_count(lib().tfl_copy_draft(t.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), len(t), int(max_draft),
+                                          out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))))
+    return out[:n]
+
+
+def _check_count(code: int) -> int:
+    if code < 0:
+        raise TflError(code, lib().tfl_last_error().decode())
+    return code
+
+
+def tfl_decode_drafted(model: Model, kv: KV, context, n_tokens: int, draft_len: int, drafter: Model = None,
+                       dkv: KV = None, stream=None):
+    ctx = np.ascontiguousarray(np.asarray(context, dtype=np.int32))
+    out = np.full(int(n_tokens), -1, np.int32)
+    nbytes = int(lib().tfl_drafted_workspace_bytes(model.handle, int(draft_len)))
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+    st = tfl_draft_stats()
+    i32 = ctypes.POINTER(ctypes.c_int32)
+    code = lib().tfl_decode_drafted(model.handle, kv.handle, drafter.handle if drafter is not None else None,
+                                    dkv.handle if dkv is not None else None, int(draft_len),
+                                    ctx.ctypes.data_as(i32), len(ctx), int(n_tokens), out.ctypes.data_as(i32),
+                                    _ptr(ws), nbytes, ctypes.byref(st), _stream(stream))
+    stats = {k: int(getattr(st, k)) for k, _ in tfl_draft_stats._fields_}
+    if code != TFL_OK:
+        err = TflError(code, lib().tfl_last_error().decode())
+        err.ids, err.stats = out, stats
+        raise err
+    return out, stats
 
 
 STEP_PHASES = ("qkv", "attention", "merge", "o", "gate_up", "down", "barrier", "head", "total")

@@ -272,6 +272,70 @@ int tfl_argmax(tfl_model* model, const void* logits, int n_rows, int32_t* ids, v
 int tfl_sample(tfl_model* model, const void* logits, int n_rows, float temperature, int top_k, float top_p,
                const float* u, int32_t* ids, void* stream);
 
+/* ---- drafted greedy decode ---------------------------------------------- */
+
+/*
+ * Drafted greedy decode (the pages: a smaller Llama on the same tokenizer
+ * drafting for the served model, "--drafter", with drafted greedy replies equal
+ * to plain greedy ones; issue #1414, reply "Drafting", and pull request #1415,
+ * section "How", whose lane host also makes "copy drafts").  Each round a
+ * proposer guesses up to draft_len next tokens, the served model runs the
+ * pending token and the guesses as one causal window, and the guesses that
+ * equal the window's own greedy ids, up to the first that does not, are kept
+ * together with the window's greedy id after them.  Because a window row is
+ * bit-identical to a one-row step (tfl_decode_step), the ids produced are
+ * exactly those of plain greedy decoding, whatever the proposer guesses.
+ *
+ * context: host int32 [n_context] (n_context >= 1), the tokens so far; the
+ * last one is pending (not yet run): length(kv) must be n_context - 1.
+ * Writes n_tokens >= 1 greedy ids to out_ids (host int32 [n_tokens]): out_ids[0]
+ * is the served model's greedy id after the pending token, and so on, as n_tokens
+ * plain one-row steps each fed the previous id would give.  On return
+ * length(kv) = n_context - 1 + n_tokens (out_ids[n_tokens - 1] is pending).
+ * kv's capacity must hold that length.
+ *
+ * Proposer: drafter != NULL: a model of the same vocabulary with its own cache
+ * dkv, holding the first length(dkv) tokens of context, n_context - length(dkv)
+ * in 1..min(16, drafter max_decode_rows); its greedy one-row steps propose the
+ * guesses (a non-finite drafter row proposes id 0).  drafter == NULL (dkv
+ * ignored): copy drafts, tfl_copy_draft over the tokens so far.  On return
+ * dkv holds a prefix of the tokens (its contents only affect speed).
+ *
+ * draft_len: 1 .. min(16, target max_decode_rows) - 1.  workspace: device,
+ * tfl_drafted_workspace_bytes(target, draft_len) bytes, 256-byte aligned,
+ * caller-owned.  stats (NULL = none): rounds, guesses made, guesses kept, rows
+ * run by the served model and by the drafter.
+ *
+ * Synchronous: each round reads the window's ids back to the host (one stream
+ * synchronisation per round).  Errors: TFL_E_ARG / TFL_E_CAPACITY / TFL_E_WORKSPACE
+ * before anything runs; TFL_E_NONFINITE when a served-model id is -1 (a NaN or
+ * +-Inf logit): out_ids holds the ids up to and including that -1, the rest
+ * are -1, and the caches hold the tokens before it.
+ */
+typedef struct {
+    long long rounds;        /* windows run by the served model */
+    long long drafted;       /* guesses proposed */
+    long long accepted;      /* guesses kept */
+    long long target_rows;   /* rows run by the served model */
+    long long drafter_rows;  /* rows run by the drafter */
+} tfl_draft_stats;
+
+size_t tfl_drafted_workspace_bytes(const tfl_model* target, int draft_len);
+int tfl_decode_drafted(tfl_model* target, tfl_kv* kv, tfl_model* drafter, tfl_kv* dkv, int draft_len,
+                       const int32_t* context, int n_context, int n_tokens, int32_t* out_ids, void* workspace,
+                       size_t ws_bytes, tfl_draft_stats* stats, void* stream);
+
+/*
+ * Copy drafts (host only): the longest suffix of tokens[0, n) of 1..3 tokens
+ * that also occurs earlier, at its latest earlier occurrence, proposes the
+ * tokens that followed that occurrence, continued periodically past the end
+ * (a sequence that repeats with period P proposes its next tokens as the
+ * repeat).  Writes up to max_draft ids to out and returns how many (0 when no
+ * suffix recurs), or TFL_E_ARG.  The pages name copy drafts without a rule;
+ * this is the reading taken.
+ */
+int tfl_copy_draft(const int32_t* tokens, int n, int max_draft, int32_t* out);
+
 /*
  * Synchronises `stream`, reads and clears the device status word: returns
  * TFL_OK, TFL_E_NONFINITE (an argmax saw a non-finite logit) or TFL_E_DEVICE
