@@ -295,7 +295,7 @@ def run_tfl(args, world, rank, local):
     shape = SHAPE.with_layers(args.layers)
     ctx = args.context
     extra = args.warmup + args.steps + 16 + 16 + 18 + 8  # warm-up, timed, profiled, e2e, per-launch steps
-    extra = max(extra, args.drafted_tokens + 1)        # the drafted-decode caches hold prompt + reply
+    extra = max(extra, args.drafted_tokens + 17)       # the drafted-decode caches hold prompt + reply
     max_ctx = ctx + extra
     dev = torch.device("cuda", torch.cuda.current_device())
 
@@ -484,7 +484,7 @@ def drafted_figures(model, kv, ids, first_id, ctx, n, dev):
     shape = model.shape
     prompt = [int(x) for x in ids.cpu()]
     context = prompt + [first_id]
-    cap = ctx + n + 1
+    cap = ctx + max(n, 16) + 1
 
     def cache_from_prompt():
         c = model.kv(cap)
@@ -506,6 +506,32 @@ def drafted_figures(model, kv, ids, first_id, ctx, n, dev):
     del kvp
     res = {"tokens": n, "plain_tok_s": round(n / plain_s, 2),
            "reply_distinct_ids": int(len(set(ref.tolist())))}
+
+    # the served model's cost of one verification window of R rows (pending token
+    # + R - 1 guesses) at this context: device time of decode step + argmax
+    st = torch.cuda.current_stream()
+    win = {}
+    wc = cache_from_prompt()
+    wid = torch.tensor(context[-16:], dtype=torch.int32, device=dev)
+    wlg = torch.empty((16, V), dtype=torch.bfloat16, device=dev)
+    wout = torch.empty(16, dtype=torch.int32, device=dev)
+    for R in (1, 2, 4, 8, 16):
+        times = []
+        for rep in range(4):
+            wc.reset(ctx)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            model.decode_step([wc], wid[:R].contiguous(), [R], wlg[:R])
+            model.argmax(wlg[:R], wout[:R])
+            e1.record(st)
+            torch.cuda.synchronize()
+            if rep:
+                times.append(e0.elapsed_time(e1))
+        win[R] = round(min(times), 4)
+    del wc
+    res["window_ms"] = win
+    # derived, not measured: tok/s if every guess of a k-guess window were kept
+    res["tok_s_if_all_kept"] = {k: round((k + 1) / win[k + 1] * 1e3, 1) for k in (1, 3, 7, 15)}
 
     dshape = shape.with_layers(DRAFTER_LAYERS)
     dw = synth.model_weights(dshape, 23, dev)
