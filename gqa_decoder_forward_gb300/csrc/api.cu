@@ -542,6 +542,15 @@ int run_step_persistent(tfl_model* m, tfl_kv* const* kvs, const RowMap& rm, cons
     a.ids = ids;
     a.logits = (bf16*)logits;
     a.rows = rm;
+    a.attn.q = m->q;
+    a.attn.out = m->ao;
+    a.attn.pm = m->pm;
+    a.attn.pl = m->pl;
+    a.attn.po = m->po;
+    a.attn.max_blocks = m->L.max_blocks;
+    a.attn.n_q = c.n_q;
+    a.attn.n_kv = c.n_kv;
+    a.attn.rows = rm;
     for (int s = 0; s < rm.n_streams; ++s) a.kvmap[s] = kvs[s]->kvmap;
     a.ts = (m->prof && m->grid <= kStepTsCtas) ? m->ts : nullptr;
     LAUNCH(m, K_STEP, st, launch_step_persistent(a, m->grid, st));

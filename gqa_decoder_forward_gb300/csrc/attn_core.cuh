@@ -37,9 +37,11 @@ constexpr int kSub = kPage;          // keys per sub-block
 constexpr int kUnit = kAttnUnit;     // keys per unit (one partial per (row, head, unit))
 constexpr int kGroupRows = 2;        // rows per group: G * 2 <= 16 (row, head) pairs, one m16 tile
 constexpr int kPairs = 16;
-constexpr int kCombFloats = kWarps * kPairs * kHeadDim + 2 * kWarps * kPairs;  // combine scratch (16 pairs)
+// combine scratch per pair: the warps' outputs, maxima, sums and weights, and M
+constexpr int kCombPerPair = kWarps * kHeadDim + 3 * kWarps + 1;
+constexpr int kCombFloats = kCombPerPair * kPairs;  // 16 pairs
 // floats of combine scratch for P pairs
-__host__ __device__ constexpr int comb_floats(int P) { return (kWarps * kHeadDim + 2 * kWarps) * ((P + 7) / 8) * 8; }
+__host__ __device__ constexpr int comb_floats(int P) { return kCombPerPair * ((P + 7) / 8) * 8; }
 
 struct UnitGeom {
     int u, g;        // unit, KV head
@@ -201,6 +203,8 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
     float* co = comb;                                   // [warp][pair][dim]
     float* cm = comb + kWarps * PS * kHeadDim;          // [warp][pair]
     float* cl = cm + kWarps * PS;
+    float* cw = cl + kWarps * PS;                       // [warp][pair]: 2^(m_w - M)
+    float* cM = cw + kWarps * PS;                       // [pair]: M
 #pragma unroll
     for (int nt = 0; nt < NP; ++nt) {
 #pragma unroll
@@ -220,19 +224,29 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
         }
     }
     bar();
+    // one thread per (warp, pair): M = max_w m_w and the weight a_w = 2^(m_w - M)
+    if (tid < kWarps * PS) {
+        const int w = tid / PS, p = tid % PS;
+        if (p < P) {
+            float M = cm[p];
+#pragma unroll
+            for (int v = 1; v < kWarps; ++v) M = fmaxf(M, cm[v * PS + p]);
+            const float mw = cm[w * PS + p];
+            cw[w * PS + p] = (M == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            if (w == 0) cM[p] = M;
+        }
+    }
+    bar();
     const int d = tid & (kHeadDim - 1);
     for (int p = tid >> 7; p < P; p += 2) {
-        float M = cm[p];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) M = fmaxf(M, cm[w * PS + p]);
+        const float M = cM[p];
         float O = 0.f, L = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float mw = cm[w * PS + p];
-                const float aw = mw == -INFINITY ? 0.f : exp2f(mw - M);
-                O = fmaf(co[((size_t)w * PS + p) * kHeadDim + d], aw, O);
-                L = fmaf(cl[w * PS + p], aw, L);
+            for (int w = 0; w < kWarps; ++w) O = fmaf(co[((size_t)w * PS + p) * kHeadDim + d], cw[w * PS + p], O);
+            if (d == 0) {
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) L = fmaf(cl[w * PS + p], cw[w * PS + p], L);
             }
         }
         const int row = ug.r0 + p / G, head = ug.g * G + p % G;
@@ -292,26 +306,60 @@ __device__ __forceinline__ float2 merge_quarter(const AttnDecodeArgs& a, size_t 
 
 // The merge of (row, head) by T threads (T = 256: quarters q and q+2 per thread;
 // T = 512: one quarter per thread).  Shared scratch: red (T / 32 floats), part
-// (kQuarters x 128 float2).  bar(): barrier of the T threads.
+// (kQuarters x 128 float2), and optionally stage (kMergeStageFloats, 16-byte
+// aligned), which lets rows of up to 32 units fetch all their partials at
+// once.  bar(): barrier of the T threads.
+constexpr int kMergeStageFloats = 8 * kQuarters * (kHeadDim + 2);
 template <int T, class Bar>
 __device__ __forceinline__ void merge(const AttnDecodeArgs& a, int row, int head, int tid, float* red, float2* part,
-                                      Bar bar) {
+                                      Bar bar, float* stage = nullptr) {
     static_assert(T == 256 || T == 512, "256 or 512 threads");
     const int d = tid & (kHeadDim - 1), q0 = tid / kHeadDim;
     const int s = row_stream(a.rows, row);
     const int pos = a.rows.pos0[s] + (row - a.rows.row_start[s]);
     const int nu = pos / kUnit + 1;
     const size_t base = ((size_t)row * a.n_q + head) * a.max_blocks;
-    float M = -INFINITY;
-    for (int u = tid; u < nu; u += T) M = fmaxf(M, a.pm[base + u]);
+    if (stage && nu <= 8 * kQuarters) {
+        // up to 32 units: every partial of the (row, head) is copied into
+        // shared memory at once (one round trip, no registers held), then
+        // folded exactly as below
+        float* so = stage;                   // [nu][128]
+        float* sm = stage + nu * kHeadDim;   // [nu] m_u
+        float* sl = sm + 8 * kQuarters;      // [nu] l_u
+        for (int i = tid; i < nu * (kHeadDim / 4); i += T)
+            wm::cp_async16_zfill(so + i * 4, a.po + base * kHeadDim + i * 4, true);
+        wm::cp_async_commit();
+        if (tid < nu)
+            sm[tid] = a.pm[base + tid];
+        else if (tid >= 32 && tid < 32 + nu)
+            sl[tid - 32] = a.pl[base + tid - 32];
+        wm::cp_async_wait_all();
+        bar();
+        float M = -INFINITY;
+        for (int u = 0; u < nu; ++u) M = fmaxf(M, sm[u]);
+        for (int q = q0; q < kQuarters; q += T / kHeadDim) {
+            const int u1 = (q + 1) * nu / kQuarters;
+            float O = 0.f, L = 0.f;
+            for (int u = q * nu / kQuarters; u < u1; ++u) {
+                const float w = exp2f(sm[u] - M);
+                L = fmaf(sl[u], w, L);
+                O = fmaf(so[u * kHeadDim + d], w, O);
+            }
+            part[q * kHeadDim + d] = make_float2(O, L);
+        }
+    } else {
+        float M = -INFINITY;
+        for (int u = tid; u < nu; u += T) M = fmaxf(M, a.pm[base + u]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if ((tid & 31) == 0) red[tid >> 5] = M;
-    bar();
-    M = red[0];
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        if ((tid & 31) == 0) red[tid >> 5] = M;
+        bar();
+        M = red[0];
 #pragma unroll
-    for (int w = 1; w < T / 32; ++w) M = fmaxf(M, red[w]);
-    for (int q = q0; q < kQuarters; q += T / kHeadDim) part[q * kHeadDim + d] = merge_quarter(a, base, nu, M, q, d);
+        for (int w = 1; w < T / 32; ++w) M = fmaxf(M, red[w]);
+        for (int q = q0; q < kQuarters; q += T / kHeadDim)
+            part[q * kHeadDim + d] = merge_quarter(a, base, nu, M, q, d);
+    }
     bar();
     if (tid < kHeadDim) {
         float O = part[d].x, L = part[d].y;

@@ -42,7 +42,7 @@ constexpr int kSub = attn::kSub;
 constexpr int kUnit = attn::kUnit;
 using attn::swz;
 
-// 201,728 bytes (one CTA per SM): queries, two buffers of one sub-block's
+// 202,304 bytes (one CTA per SM): queries, two buffers of one sub-block's
 // keys and values each (sub-block j+1 streams in while j is computed), and the
 // scratch that combines the eight warp partials.
 struct Smem {

@@ -179,6 +179,7 @@ struct StepArgs {
     const int32_t* ids;         // device, n_rows
     bf16* logits;               // device [n_rows][V]
     RowMap rows;
+    AttnDecodeArgs attn;        // the attention's view of q, ao, the partials and rows (layer unused)
     unsigned long long* ts;     // optional (NULL: off): per CTA, kStepTsStride global-timer stamps
     CUtensorMap kvmap[kStepMaxRows];  // per stream: 3-D map over the cache pages (128 dims, n_kv, rows)
 };

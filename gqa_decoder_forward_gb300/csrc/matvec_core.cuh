@@ -119,7 +119,8 @@ struct NamedBar1 {
 // consumer threads.  After a failed wait the loop keeps walking (no more waits)
 // so that every consumer reaches the barriers.
 template <int NT, class XFrag, class Bar>
-__device__ __forceinline__ void consume_tile(const MatvecArgs& e, int t, int nst, int R, uint32_t base_u,
+__device__ __forceinline__ void consume_tile(const MatvecArgs& e, const RowMap& rows, int t, int nst, int R,
+                                             uint32_t base_u,
                                              int stage_bytes, int depth, int& stage, uint32_t& phase, uint64_t* full,
                                              uint64_t* empty, float* red, volatile int* s_abort, int* status,
                                              XFrag xfrag, Bar bar) {
@@ -173,8 +174,8 @@ __device__ __forceinline__ void consume_tile(const MatvecArgs& e, int t, int nst
         }
         // c0 = (lo g, row 2tig), c1 = (lo g, row 2tig+1), c2 = (hi g, row 2tig), c3 = (hi g, row 2tig+1)
         const int r0 = n * 8 + 2 * tig;
-        if (r0 < R) mv::epilogue(e, tr, g, r0, v[0], v[2]);
-        if (r0 + 1 < R) mv::epilogue(e, tr, g, r0 + 1, v[1], v[3]);
+        if (r0 < R) mv::epilogue(e, rows, tr, g, r0, v[0], v[2]);
+        if (r0 + 1 < R) mv::epilogue(e, rows, tr, g, r0 + 1, v[1], v[3]);
     }
     bar();
 }

@@ -20,8 +20,8 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 // Epilogue of one (feature pair, activation row): vlo/vhi are the fp32 sums of
 // the lo-group row g and the hi-group row g for activation row r.
-__device__ __forceinline__ void epilogue(const MatvecArgs& a, const TileRows& tr, int g, int r, float vlo,
-                                         float vhi) {
+__device__ __forceinline__ void epilogue(const MatvecArgs& a, const RowMap& rows, const TileRows& tr, int g, int r,
+                                         float vlo, float vhi) {
     if (a.mode == MV_STORE) {
         bf16* y = a.y + (size_t)r * a.ldy + tr.j0;
         y[g] = rn(vlo);
@@ -36,8 +36,8 @@ __device__ __forceinline__ void epilogue(const MatvecArgs& a, const TileRows& tr
     } else {  // MV_QKV_ROPE
         const int jl = tr.j0 + g, jh = jl + 64;
         float xl = rbf(vlo), xh = rbf(vhi);
-        const int s = row_stream(a.rows, r);
-        const int pos = a.rows.pos0[s] + (r - a.rows.row_start[s]);
+        const int s = row_stream(rows, r);
+        const int pos = rows.pos0[s] + (r - rows.row_start[s]);
         bf16 ol, oh;
         if (tr.seg < 2) {
             float c = bf(a.cos_t[(size_t)pos * 64 + jl]);
@@ -53,7 +53,7 @@ __device__ __forceinline__ void epilogue(const MatvecArgs& a, const TileRows& tr
             q[jl] = ol;
             q[jh] = oh;
         } else {
-            bf16* row = kv_row(a.rows.kv[s], a.layer, tr.seg - 1, pos, a.n_kv) + (size_t)tr.head * kHeadDim;
+            bf16* row = kv_row(rows.kv[s], a.layer, tr.seg - 1, pos, a.n_kv) + (size_t)tr.head * kHeadDim;
             row[jl] = ol;
             row[jh] = oh;
         }

@@ -149,10 +149,10 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
     uint32_t phase = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
         if (NORM)
-            mvc::consume_tile<NT>(a.e, t, nst, R, base_u, stage_bytes, depth, stage, phase, full, empty, red, s_abort,
+            mvc::consume_tile<NT>(a.e, a.e.rows, t, nst, R, base_u, stage_bytes, depth, stage, phase, full, empty, red, s_abort,
                                   a.status, mvc::XFromLines{xn_u, R, kblocks, tig}, bar);
         else
-            mvc::consume_tile<NT>(a.e, t, nst, R, base_u, stage_bytes, depth, stage, phase, full, empty, red, s_abort,
+            mvc::consume_tile<NT>(a.e, a.e.rows, t, nst, R, base_u, stage_bytes, depth, stage, phase, full, empty, red, s_abort,
                                   a.status, mvc::XFromStage{xrows, warp, tig}, bar);
     }
 }

@@ -49,6 +49,12 @@ constexpr int kMaxDepth = 8;
 __host__ __device__ constexpr int ring_depth(int) { return 8; }
 __host__ __device__ constexpr int xs_bytes(int rows) { return rows * 22016 * 2; }  // down-projection lines
 constexpr int kStage = kABytes;                       // 16 KB: one weight stage or one K/V tile
+// the activation space also holds the attention's queries and combine scratch,
+// and the merge's scratch and staged partials
+static_assert(attn::kPairs * kHeadDim * 2 + attn::comb_floats(attn::kGroupRows * 8) * 4 <= xs_bytes(kStepMaxRows),
+              "attention scratch exceeds the activation space");
+static_assert(attn::comb_floats(8) * 4 + attn::kPairs * kHeadDim * 2 <= xs_bytes(1), "one-row attention scratch");
+static_assert(8192 + attn::kMergeStageFloats * 4 <= xs_bytes(1), "merge scratch exceeds the activation space");
 constexpr int kRedBytes = kConsumerWarps * 4 * 32 * 4;
 constexpr int kPhasesPerLayer = 6;
 constexpr uint32_t kSpinLimit = 1u << 24;
@@ -76,7 +82,6 @@ __device__ __forceinline__ MatvecArgs phase_args(const StepArgs& a, int l, int p
             e.cos_t = a.cos_t;
             e.sin_t = a.sin_t;
             e.layer = l;
-            e.rows = a.rows;
             break;
         case PH_O:
             e.mode = MV_RESIDUAL;
@@ -378,16 +383,7 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
     RingPos rp{0, 0u, ring_depth(a.rows.n_rows)};
     unsigned epoch = 0;
     const int nblk = attn_blocks(a), units = nblk * a.n_kv * attn_groups(a);
-    AttnDecodeArgs at = {};
-    at.q = a.q;
-    at.out = a.ao;
-    at.pm = a.pm;
-    at.pl = a.pl;
-    at.po = a.po;
-    at.max_blocks = a.max_blocks;
-    at.n_q = a.n_q;
-    at.n_kv = a.n_kv;
-    at.rows = a.rows;
+    const AttnDecodeArgs& at = a.attn;
 
     unsigned long long* ts = a.ts ? a.ts + (size_t)blockIdx.x * step_ts_stride(a.layers) : nullptr;
     auto stamp = [&](int i) {
@@ -415,7 +411,7 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
         const int tiles = phase_tiles(e), nst = (e.K + 511) / 512, kblocks = e.K / 64;
         mvc::rows_to_lines(row, norm_w, a.eps, R, e.K, xs_u, red_norm, bar);
         for (int t = blockIdx.x; t < tiles; t += G)
-            mvc::consume_tile<1>(e, t, nst, R, ring_u, kStage, rp.depth, rp.stage, rp.phase, full, empty, red, s_abort,
+            mvc::consume_tile<1>(e, a.rows, t, nst, R, ring_u, kStage, rp.depth, rp.stage, rp.phase, full, empty, red, s_abort,
                                  a.status, mvc::XFromLines{xs_u, R, kblocks, tig}, bar);
     };
     auto hrow = [&](int r) { return (const bf16*)a.h + (size_t)r * a.H; };
@@ -446,7 +442,6 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
         }
         if (!grid_barrier()) return;
         // attention block partials: blocks written by earlier steps, then this step's
-        at.layer = l;
         for (int pass = 0; pass < 2; ++pass)
             for (int u = blockIdx.x; u < units; u += G) {
                 Unit x;
@@ -463,8 +458,9 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
         {
             float* redm = reinterpret_cast<float*>(xs);
             float2* part = reinterpret_cast<float2*>(xs + 64);
+            float* stage = reinterpret_cast<float*>(xs + 8192);
             for (int u = blockIdx.x; u < R * a.n_q; u += G)
-                attn::merge<kConsumerWarps * 32>(at, u / a.n_q, u % a.n_q, tid, redm, part, bar);
+                attn::merge<kConsumerWarps * 32>(at, u / a.n_q, u % a.n_q, tid, redm, part, bar, stage);
         }
         if (!grid_barrier()) return;
         matvec(l, PH_O, aorow, nullptr);
