@@ -111,19 +111,18 @@ struct NamedBar1 {
     __device__ __forceinline__ void operator()() const { named_barrier(1, kConsumerWarps * 32); }
 };
 
-// Accumulates tile t over its nst stages (consumer warps 0..7 of the CTA, ring
-// of `depth` stages of stage_bytes at base_u), then sums the eight warps in
-// order and runs the epilogue for the R activation rows.  xfrag(xr, kb, sX, x0,
-// x1) fills the B fragment (16-byte chunks tig and tig+4 of k-block kb) of
-// activation row xr (< 8 * NT), or leaves it zero.  bar() synchronises the 256
-// consumer threads.  After a failed wait the loop keeps walking (no more waits)
-// so that every consumer reaches the barriers.
-template <int NT, class XFrag, class Bar>
-__device__ __forceinline__ void consume_tile(const MatvecArgs& e, const RowMap& rows, int t, int nst, int R,
-                                             uint32_t base_u,
-                                             int stage_bytes, int depth, int& stage, uint32_t& phase, uint64_t* full,
-                                             uint64_t* empty, float* red, volatile int* s_abort, int* status,
-                                             XFrag xfrag, Bar bar) {
+
+// Accumulates stages ks0 .. ks1-1 of a tile into acc (consumer warps 0..7 of
+// the CTA, ring of `depth` stages of stage_bytes at base_u): warp w takes
+// k-block w of every stage.  xfrag(xr, kb, sX, x0, x1) fills the B fragment
+// (16-byte chunks tig and tig+4 of k-block kb) of activation row xr (< 8 * NT),
+// or leaves it zero.  After a failed wait the loop keeps walking (no more
+// waits) so that every consumer reaches the barriers.
+template <int NT, class XFrag>
+__device__ __forceinline__ void accumulate_stages(const MatvecArgs& e, float (&acc)[NT][4], int ks0, int ks1,
+                                                  uint32_t base_u, int stage_bytes, int depth, int& stage,
+                                                  uint32_t& phase, uint64_t* full, uint64_t* empty,
+                                                  volatile int* s_abort, int* status, XFrag xfrag) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, tig = lane & 3;
     // line of this warp's lo / hi weight row inside a stage: [k-block][16 rows]
@@ -131,10 +130,7 @@ __device__ __forceinline__ void consume_tile(const MatvecArgs& e, const RowMap& 
     const bool two_boxes = e.mode == MV_SWIGLU || e.mode == MV_QKV_ROPE;
     const int line_lo = two_boxes ? warp * 8 + g : warp * 16 + g;
     const int line_hi = two_boxes ? (kABytes / 2) / 128 + warp * 8 + g : warp * 16 + 8 + g;
-    float acc[NT][4];
-#pragma unroll
-    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-    for (int ks = 0; ks < nst; ++ks) {
+    for (int ks = ks0; ks < ks1; ++ks) {
         if (!*s_abort && !mbar_wait(&full[stage], phase, status)) *s_abort = 1;
         const uint32_t sA = base_u + stage * stage_bytes;
         const uint32_t sX = sA + kABytes;
@@ -156,7 +152,15 @@ __device__ __forceinline__ void consume_tile(const MatvecArgs& e, const RowMap& 
         if (lane == 0) mbar_arrive(&empty[stage]);
         if (++stage == depth) { stage = 0; phase ^= 1u; }
     }
-    // fixed-order sum over the eight warps, then the epilogue
+}
+
+// Sums the eight warps' accumulators of tile t in warp order and runs the
+// epilogue for the R activation rows.  bar() synchronises the 256 consumer threads.
+template <int NT, class Bar>
+__device__ __forceinline__ void finish_tile(const MatvecArgs& e, const RowMap& rows, int t, int R,
+                                            const float (&acc)[NT][4], float* red, Bar bar) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
 #pragma unroll
     for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -180,6 +184,20 @@ __device__ __forceinline__ void consume_tile(const MatvecArgs& e, const RowMap& 
     bar();
 }
 
+// One whole tile t over its nst stages: accumulate_stages then finish_tile.
+template <int NT, class XFrag, class Bar>
+__device__ __forceinline__ void consume_tile(const MatvecArgs& e, const RowMap& rows, int t, int nst, int R,
+                                             uint32_t base_u, int stage_bytes, int depth, int& stage, uint32_t& phase,
+                                             uint64_t* full, uint64_t* empty, float* red, volatile int* s_abort,
+                                             int* status, XFrag xfrag, Bar bar) {
+    float acc[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+    accumulate_stages<NT>(e, acc, 0, nst, base_u, stage_bytes, depth, stage, phase, full, empty, s_abort, status,
+                          xfrag);
+    finish_tile<NT>(e, rows, t, R, acc, red, bar);
+}
+
 // Activation rows (R rows of K bf16, row r at row(r), optionally RMSNormed
 // with norm_w) into shared lines [k-block][row][64] (line l = kb * R + r, chunk
 // c of line l at chunk c ^ (l mod 8)), by the 256 consumer threads.  The norm
@@ -189,6 +207,12 @@ template <class RowPtr, class Bar>
 __device__ __forceinline__ void rows_to_lines(RowPtr row, const bf16* norm_w, float eps, int R, int K, uint32_t xs_u,
                                               float* red_norm, Bar bar) {
     const int tid = threadIdx.x;
+    auto put = [&](int i, int r, const uint4& o) {
+        const int line = (i >> 6) * R + r, c = (i & 63) >> 3;
+        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xs_u + line * 128 + ((c ^ (line & 7)) << 4)),
+                     "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
+                     : "memory");
+    };
     for (int r = 0; r < R; ++r) {
         const bf16* hr = row(r);
         const float rinv = norm_w ? rms_inv(hr, K, eps, tid, red_norm + r * 8, bar) : 0.f;
@@ -204,10 +228,7 @@ __device__ __forceinline__ void rows_to_lines(RowPtr row, const bf16* norm_w, fl
                 for (int k = 0; k < 8; ++k) ne[k] = rms_apply(he[k], we[k], rinv);
                 o = n;
             }
-            const int line = (i >> 6) * R + r, c = (i & 63) >> 3;
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(xs_u + line * 128 + ((c ^ (line & 7)) << 4)),
-                         "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
-                         : "memory");
+            put(i, r, o);
         }
     }
     bar();
