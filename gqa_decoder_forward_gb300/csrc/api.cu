@@ -602,11 +602,14 @@ cudaError_t gemm_launch(tfl_model* m, const MatvecArgs& e, const CUtensorMap* am
 
 // Causal attention of the rows of a prompt chunk (one stream, queries q,
 // output out, both [rows][n_q*128]) in one launch of the prefill kernel.
-int prompt_attention(tfl_model* m, const RowMap& rm, int layer, const bf16* q, bf16* out, cudaStream_t st,
-                     bool pdl) {
+int prompt_attention(tfl_model* m, const tfl_kv* kv, const RowMap& rm, int layer, const bf16* q, bf16* out,
+                     cudaStream_t st, bool pdl) {
     const tfl_config& c = m->cfg;
     AttnPrefillArgs p = {};
-    p.q = q;
+    if (!encode_map2d(&p.qmap, q, (uint64_t)c.n_q * kHeadDim, (uint64_t)rm.n_rows, 128))
+        return fail(TFL_E_ARG, "cannot describe the query rows to TMA");
+    p.kvmap = kv->kvmap;
+    p.status = m->status;
     p.out = out;
     p.kv = rm.kv[0];
     p.n_q = c.n_q;
@@ -622,7 +625,8 @@ int prompt_attention(tfl_model* m, const RowMap& rm, int layer, const bf16* q, b
 // tcgen05 GEMM projections with fused epilogues, attention.  Each row's result
 // depends only on its own input and position, so chunk boundaries never change
 // results (a prompt resumed from a kept prefix equals the same prompt fresh).
-int run_prompt_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h_in, cudaStream_t st) {
+int run_prompt_layers(tfl_model* m, const tfl_kv* kv, const RowMap& rm, const int32_t* ids, const void* h_in,
+                      cudaStream_t st) {
     const tfl_config& c = m->cfg;
     const int n = rm.n_rows, H = c.hidden, qd = c.n_q * kHeadDim;
     const bool pdl = m->pdl && st != nullptr;
@@ -650,7 +654,7 @@ int run_prompt_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const 
         a.layer = l;
         a.rows = rm;
         LAUNCH(m, K_GQKV, st, gemm_launch(m, a, &m->amap_xn, &wm.gq, &wm.gk, &wm.gv, st, pdl));
-        int e = prompt_attention(m, rm, l, m->q, m->ao, st, pdl);
+        int e = prompt_attention(m, kv, rm, l, m->q, m->ao, st, pdl);
         if (e) return e;
         MatvecArgs o = {};
         o.mode = MV_RESIDUAL;
@@ -694,7 +698,7 @@ int prefill_common(tfl_model* m, tfl_kv* kv, const int32_t* ids, const void* h_i
     rm.row_start[1] = n_rows;
     rm.pos0[0] = kv->length;
     rm.kv[0] = view(kv);
-    int e = run_prompt_layers(m, rm, ids, h_in, st);
+    int e = run_prompt_layers(m, kv, rm, ids, h_in, st);
     if (e) return e;
     if (h_out) CK(cudaMemcpyAsync(h_out, m->h, (size_t)n_rows * H * 2, cudaMemcpyDeviceToDevice, st));
     if (logits && all_rows) {
@@ -1208,7 +1212,7 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             at.layer = layer;
             at.rows = rm;
             if (prompt) {
-                const int e = prompt_attention(m, rm, layer, (const bf16*)in, (bf16*)out, st, false);
+                const int e = prompt_attention(m, kv, rm, layer, (const bf16*)in, (bf16*)out, st, false);
                 if (e) return e;
                 break;
             }

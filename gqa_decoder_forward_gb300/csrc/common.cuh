@@ -151,11 +151,13 @@ cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl
 // Causal attention of the rows of one prompt chunk (one stream): row r at
 // position pos0 + r attends keys 0 .. pos0 + r of kv (layer).
 struct AttnPrefillArgs {
-    const bf16* q;        // [n_rows][n_q*D] rotated
+    CUtensorMap qmap;     // q [n_rows][n_q*D] rotated: 2-D, boxes of 64 columns x 128 rows, 128-byte swizzle
+    CUtensorMap kvmap;    // the cache's pages (the tfl_kv's 3-D map: 64 dims x 1 head x 128 positions)
     bf16* out;            // [n_rows][n_q*D]
     KvView kv;
     int n_q, n_kv, layer;
     int pos0, n_rows;
+    int* status;
 };
 cudaError_t init_attn_prefill();
 cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t st, bool pdl);
