@@ -3,52 +3,64 @@
 // and the chunk's own earlier rows on the tensor units), one pass with an
 // online softmax, the products on the 5th-generation tensor cores.
 //
-// One CTA per (query head h, tile of 128 consecutive rows), 192 threads:
-//   warp 0   TMA producer: the tile's queries once, then the keys and values of
-//            KV head h / G block by block (a block = 128 positions = one cache
-//            page), double-buffered;
-//   warp 1   allocates tensor memory and issues the MMAs (one thread):
-//            S = Q K^T into tensor memory (M = 128 rows, N = 128 keys, fp32),
-//            then O_blk = P_hi V + P_lo V (M = 128 rows, N = 128 dims) with the
-//            weights P from shared memory and V read MN-major;
-//   warps 2-5 one query row per thread (tensor-memory lane = row): read the
-//            row of S, causal mask, block max, weights p = 2^(s - m_new) as a
-//            pair of bf16 numbers into shared memory, running sum; then fold
-//            the block's O_blk into the row's fp32 output in registers,
-//            O = O 2^(m_old - m_new) + O_blk; at the end out = bf16(O / l).
-// The next block's S = Q K^T is issued before this block's P V, and a row's
-// max pass over the next block runs while P V is in flight.
+// One CTA per (query head h, pair of 128-row tiles A and B), 320 threads:
+//   warps 0-3 softmax of tile A, warps 4-7 softmax of tile B: one query row
+//            per thread (tensor-memory lane = row of the tile);
+//   warp 8   TMA producer: both tiles' queries once, then the keys and values
+//            of KV head h / G block by block (a block = 128 positions = one
+//            cache page), double-buffered;
+//   warp 9   allocates tensor memory and issues the MMAs (one thread), per
+//            block and tile: S = Q K^T (M = 128 rows, N = 128 keys, fp32 in
+//            tensor memory), then O += P V (M = 128 rows, N = 128 dims) with the
+//            weights P read from tensor memory, where the softmax wrote them
+//            over S, and V read MN-major from shared memory.
+// While one tile's rows run their softmax, the tensor cores work on the other
+// tile, and both tiles share each key/value block.
 //
-// Precision: scores are fp32 dot products of the bf16 q and k, scaled by
-// log2(e)/sqrt(128) in fp32 so that exp2 gives e^(score/sqrt(128)); weights are
-// fp32 and enter P V as hi = bf16(p) and lo = bf16(p - hi) (about 16
-// significant bits) -- they are not rounded to bf16.  The output is rounded
-// to bf16 once.
+// Softmax of a row over block j: scores s (fp32 dot products of the bf16 q and
+// k), visible keys only (causal), block max b = max(s) log2(e)/sqrt(128).  The
+// row keeps a reference max m; when b > m + 8 (always on the first block) the
+// reference becomes b and the running sum l and the tensor-memory output O are
+// multiplied by 2^(m_old - m_new) (exactly the online softmax, rescaled lazily:
+// every weight stays <= 2^8).  Weights p = 2^(s log2(e)/sqrt(128) - m) enter
+// P V as hi = bf16(p) and lo = bf16(p - hi) (about 16 significant bits; they
+// are not rounded to bf16); l += sum p in a fixed order.  At the end
+// out = bf16(O / l), rounded once.
 //
 // Determinism: a row's arithmetic depends only on the row and its position.
 // Key blocks sit at absolute positions and are visited in order from 0; keys
-// past a row's position have weight exactly 0 (a block past the row changes
-// nothing: the max stays, the rescale factor is 1, O_blk of the row is 0);
-// values past the tile's last position are zeroed in shared memory; every
-// product element depends only on its own row of Q or P.  Chunk boundaries and
-// a row's place in its tile change no bits (a prompt resumed from a kept prefix
-// equals the same prompt prefilled fresh).
+// past a row's position have weight exactly 0 (a block past the row adds
+// nothing and rescales nothing); values past the CTA's last position are
+// zeroed in shared memory; every product element depends only on its own row
+// of Q or P.  Chunk boundaries and a row's tile change no bits (a prompt
+// resumed from a kept prefix equals the same prompt prefilled fresh).
 #include "common.cuh"
 #include "tcgen05.cuh"
 #include "tma.cuh"
-#include "warp_mma.cuh"
 
 namespace tfl {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kBM = 128;                  // query rows per CTA
+constexpr int kThreads = 320;
+constexpr int kBM = 128;                  // query rows per tile
 constexpr int kBN = kPage;                // keys per block: one cache page
 constexpr int kBox = 128 * 64 * 2;        // 16 KB: 128 rows x 64 columns, 128-byte swizzle
 constexpr int kTile = 2 * kBox;           // 32 KB: 128 rows x 128 columns
-constexpr int kTmemCols = 256;            // S: columns 0..127, O_blk: 128..255
+constexpr int kTmemCols = 512;            // S/P of A, S/P of B, O of A, O of B: 128 columns each
 constexpr float kScale = 0.12751743074640502f;  // log2(e) / sqrt(128)
-using wm::pack_bf16;
+constexpr float kRescale = 8.f;           // lazy rescale threshold (log2 units)
+
+// Shared memory (from a 1024-byte aligned base): Q[2], K[2], V[2], barriers.
+constexpr int kOffQ = 0, kOffK = 2 * kTile, kOffV = 4 * kTile;
+constexpr int kOffBar = 6 * kTile;
+constexpr int kSmem = 1024 + kOffBar + 16 * 8;
+
+struct Bars {
+    uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], o_full[2];
+    uint32_t tmem;
+    int abort;
+};
+static_assert(sizeof(Bars) <= 16 * 8, "barrier area");
 
 // 2^x by the special-function unit (approximate, flushes subnormal results to
 // zero; 2^-inf = 0).
@@ -58,16 +70,10 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Shared memory (from a 1024-byte aligned base): Q, K[2], V[2], P_hi, P_lo, barriers.
-constexpr int kOffQ = 0, kOffK = kTile, kOffV = 3 * kTile, kOffPh = 5 * kTile, kOffPl = 6 * kTile;
-constexpr int kOffBar = 7 * kTile;
-constexpr int kSmem = 1024 + kOffBar + 16 * 8;
-
-struct Bars {
-    uint64_t q_full, kv_full[2], kv_empty[2], s_full, s_empty, p_full, o_full, o_empty;
-    uint32_t tmem;
-    int abort;
-};
+__device__ __forceinline__ uint32_t pack_rn(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
 
 // Descriptor of the K-major 128 x 128 tile at `tile` (two 64-column boxes) for k-step kk (16 columns).
 __device__ __forceinline__ uint64_t kdesc(uint32_t tile, int kk) {
@@ -82,30 +88,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
     volatile int* abort = &b.abort;
     const uint32_t su = smem_u32(base);
     const int h = blockIdx.x;
-    const int tile = gridDim.y - 1 - blockIdx.y;  // the longest tiles start first
+    const int pair = gridDim.y - 1 - blockIdx.y;  // the longest tiles start first
     const int G = a.n_q / a.n_kv, g = h / G;
-    const int r0 = tile * kBM;
-    const int nr = min(kBM, a.n_rows - r0);
-    const int p_first = a.pos0 + r0;
-    const int p_last = p_first + nr - 1;
-    const int nb = p_last / kBN + 1;  // key blocks 0 .. nb-1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // tiles A (t = 0) and B (t = 1): rows, positions, key blocks
+    int r0[2], nr[2], nbt[2], p_first[2], p_last[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        r0[t] = (2 * pair + t) * kBM;
+        nr[t] = min(kBM, a.n_rows - r0[t]);
+        p_first[t] = a.pos0 + r0[t];
+        p_last[t] = p_first[t] + nr[t] - 1;
+        nbt[t] = nr[t] > 0 ? p_last[t] / kBN + 1 : 0;
+    }
+    const int nb = max(nbt[0], nbt[1]);
+    const int p_end = nr[1] > 0 ? p_last[1] : p_last[0];  // the CTA's last position
 
     if (threadIdx.x == 0) {
         mbar_init(&b.q_full, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&b.kv_full[i], 1);
             mbar_init(&b.kv_empty[i], 1);
+            mbar_init(&b.s_full[i], 1);
+            mbar_init(&b.p_full[i], kBM);
+            mbar_init(&b.o_full[i], 1);
         }
-        mbar_init(&b.s_full, 1);
-        mbar_init(&b.s_empty, kBM);
-        mbar_init(&b.p_full, kBM);
-        mbar_init(&b.o_full, 1);
-        mbar_init(&b.o_empty, kBM);
         b.abort = 0;
         mbar_init_fence();
     }
-    if (warp == 1) {
+    if (warp == 9) {
         tmem_alloc(&b.tmem, kTmemCols);
         tmem_relinquish();
     }
@@ -115,13 +126,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
     const uint32_t tmem = b.tmem;
     pdl_wait();
 
-    if (warp == 0) {
+    if (warp == 8) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const uint64_t keep = policy_evict_last(), once = policy_evict_first();
-            mbar_arrive_expect_tx(&b.q_full, kTile);
-            tma_load_2d(base + kOffQ, &a.qmap, h * kHeadDim, r0, &b.q_full, once);
-            tma_load_2d(base + kOffQ + kBox, &a.qmap, h * kHeadDim + 64, r0, &b.q_full, once);
+            mbar_arrive_expect_tx(&b.q_full, 2 * kTile);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {  // rows past the chunk read as zeros
+                tma_load_2d(base + kOffQ + t * kTile, &a.qmap, h * kHeadDim, r0[t], &b.q_full, once);
+                tma_load_2d(base + kOffQ + t * kTile + kBox, &a.qmap, h * kHeadDim + 64, r0[t], &b.q_full, once);
+            }
             for (int j = 0; j < nb && !*abort; ++j) {
                 const int buf = j & 1;
                 if (j >= 2 && !mbar_wait(&b.kv_empty[buf], ((j >> 1) - 1) & 1, a.status)) {
@@ -139,78 +153,67 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 9) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN);
             constexpr uint32_t idPV = idesc_bf16_f32_bmn(kBM, kHeadDim);
-            const uint32_t tS = tmem, tO = tmem + 128;
-            auto issue_s = [&](int j) -> bool {
-                const int buf = j & 1;
-                if (!mbar_wait(&b.kv_full[buf], (j >> 1) & 1, a.status)) return false;
-                if (j > 0 && !mbar_wait(&b.s_empty, (j - 1) & 1, a.status)) return false;
-                tc_fence_after();
-                const uint32_t kt = su + kOffK + buf * kTile;
-#pragma unroll
-                for (int kk = 0; kk < kHeadDim / 16; ++kk)
-                    tc_mma_bf16(tS, kdesc(su + kOffQ, kk), kdesc(kt, kk), idS, kk > 0 ? 1u : 0u);
-                tc_commit(&b.s_full);
-                return true;
-            };
-            bool ok = mbar_wait(&b.q_full, 0, a.status) && issue_s(0);
+            bool ok = mbar_wait(&b.q_full, 0, a.status);
             for (int j = 0; j < nb && ok; ++j) {
                 const int buf = j & 1;
-                if (j + 1 < nb && !issue_s(j + 1)) {
-                    ok = false;
-                    break;
-                }
-                // O_blk = P_hi V + P_lo V once the weights are written and the
-                // previous O_blk has been read
-                if (!mbar_wait(&b.p_full, j & 1, a.status) || (j > 0 && !mbar_wait(&b.o_empty, (j - 1) & 1, a.status))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t vt = su + kOffV + buf * kTile;
+                ok = mbar_wait(&b.kv_full[buf], (j >> 1) & 1, a.status);
+                const uint32_t kt = su + kOffK + buf * kTile, vt = su + kOffV + buf * kTile;
+                // S = Q K^T per tile, once that tile's previous P V (which read
+                // the weights in the same columns) has finished
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    tc_mma_bf16(tO, kdesc(su + kOffPh, kk), sdesc_sw128_mn(vt + kk * 2048, kBox), idPV, kk > 0 ? 1u : 0u);
+                for (int t = 0; t < 2; ++t) {
+                    if (!ok || j >= nbt[t]) continue;
+                    if (j > 0 && !mbar_wait(&b.o_full[t], (j - 1) & 1, a.status)) {
+                        ok = false;
+                        continue;
+                    }
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    tc_mma_bf16(tO, kdesc(su + kOffPl, kk), sdesc_sw128_mn(vt + kk * 2048, kBox), idPV, 1u);
-                tc_commit(&b.o_full);
-                tc_commit(&b.kv_empty[buf]);
+                    for (int kk = 0; kk < kHeadDim / 16; ++kk)
+                        tc_mma_bf16(tmem + t * 128, kdesc(su + kOffQ + t * kTile, kk), kdesc(kt, kk), idS,
+                                    kk > 0 ? 1u : 0u);
+                    tc_commit(&b.s_full[t]);
+                }
+                // O += P_hi V + P_lo V per tile once its weights are written
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    if (!ok || j >= nbt[t]) continue;
+                    if (!mbar_wait(&b.p_full[t], j & 1, a.status)) {
+                        ok = false;
+                        continue;
+                    }
+                    tc_fence_after();
+                    const uint32_t tp = tmem + t * 128, to = tmem + 256 + t * 128;
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        tc_mma_bf16_ta(to, tp + 32 * (kk >> 1) + 8 * (kk & 1), sdesc_sw128_mn(vt + kk * 2048, kBox),
+                                       idPV, (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        tc_mma_bf16_ta(to, tp + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
+                                       sdesc_sw128_mn(vt + kk * 2048, kBox), idPV, 1u);
+                    tc_commit(&b.o_full[t]);
+                }
+                if (ok) tc_commit(&b.kv_empty[buf]);
             }
             if (!ok) *abort = 1;
         }
     } else {
         // ---------------- softmax: one row per thread ----------------
-        const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
-        const int pos = min(p_first + row, p_last);  // rows past the chunk see only real keys
-        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem + lane_off, tO = tmem + lane_off + 128;
-        float o[kHeadDim];
-#pragma unroll
-        for (int d = 0; d < kHeadDim; ++d) o[d] = 0.f;
-        float m = -INFINITY, l = 0.f, alpha_prev = 1.f;
+        const int t = warp >> 2;
+        const int row = (warp & 3) * 32 + lane;
+        const int pos = min(p_first[t] + row, p_last[t]);  // rows past the chunk see only real keys
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + lane_off + t * 128, tO = tmem + lane_off + 256 + t * 128;
+        float m = -INFINITY, l = 0.f;
         bool ok = true;
-        // O += O_blk of block j, rescaled by alpha (the factor from block j-1's max to block j's)
-        auto fold_o = [&](int j, float alpha) {
-            if (ok && !*abort && !mbar_wait(&b.o_full, j & 1, a.status)) ok = false;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < kHeadDim / 32; ++c) {
-                float v[32];
-                tmem_ld32(tO + c * 32, v);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[c * 32 + e] = fmaf(o[c * 32 + e], alpha, v[e]);
-            }
-            tc_fence_before();
-            mbar_arrive(&b.o_empty);
-        };
-        for (int j = 0; j < nb; ++j) {
-            if (ok && !*abort && !mbar_wait(&b.s_full, j & 1, a.status)) ok = false;
+        for (int j = 0; j < nbt[t]; ++j) {
+            if (ok && !*abort && !mbar_wait(&b.s_full[t], j & 1, a.status)) ok = false;
             tc_fence_after();
             const int k0 = j * kBN;
             const bool whole = k0 + kBN - 1 <= pos;  // every key of the block is visible to the row
@@ -229,12 +232,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
                         if (k0 + c * 32 + e <= pos) mx = fmaxf(mx, v[e]);
                 }
             }
-            const float m_new = fmaxf(m, mx * kScale);
-            const float alpha = ex2(m - m_new);
-            // the previous block's O_blk (P V finished, so P may be rewritten)
-            if (j > 0) fold_o(j - 1, alpha_prev);
-            // pass 2: weights p = 2^(s scale - m_new) as (hi, lo) into shared
-            // memory; four running sums over keys 4i+0..3, added in order at the end
+            const float bmax = mx * kScale;
+            const bool rescale = bmax > m + kRescale;  // a new reference max (always on block 0)
+            const float alpha = rescale ? ex2(m - bmax) : 1.f;
+            // O holds blocks 0 .. j-1 (this block's S was issued after that P V
+            // finished); tensor-memory loads and stores take the whole warp, so
+            // rows that keep their reference rewrite O times 1
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                for (int c = 0; c < kHeadDim / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(tO + c * 32, v);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(v[half * 16 + e] * alpha);
+                        tmem_st16(tO + c * 32 + half * 16, w);
+                    }
+                }
+            }
+            if (rescale) {
+                l *= alpha;
+                m = bmax;
+            }
+            // pass 2: weights (hi, lo) written over the scores; four running
+            // sums over keys 4i+0..3, added in order at the end
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < kBN / 32; ++c) {
@@ -243,36 +266,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
                 uint32_t hi[16], lo[16];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    float p0 = ex2(fmaf(v[e], kScale, -m_new)), p1 = ex2(fmaf(v[e + 1], kScale, -m_new));
+                    float p0 = ex2(fmaf(v[e], kScale, -m)), p1 = ex2(fmaf(v[e + 1], kScale, -m));
                     if (!whole) {
                         if (k0 + c * 32 + e > pos) p0 = 0.f;
                         if (k0 + c * 32 + e + 1 > pos) p1 = 0.f;
                     }
                     ls[e & 3] += p0;
                     ls[(e + 1) & 3] += p1;
-                    const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-                    const __nv_bfloat162 r = __floats2bfloat162_rn(p0 - __low2float(h), p1 - __high2float(h));
-                    hi[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
-                    lo[e / 2] = *reinterpret_cast<const uint32_t*>(&r);
+                    const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+                    hi[e / 2] = *reinterpret_cast<const uint32_t*>(&hh);
+                    lo[e / 2] = pack_rn(p0 - __low2float(hh), p1 - __high2float(hh));
                 }
-                // keys 32c .. 32c+31 = chunks 4c .. 4c+3 of the row (box c / 2)
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int ch = (4 * c + q4) & 7;
-                    const uint32_t off = (c >> 1) * kBox + row * 128 + ((ch ^ (row & 7)) << 4);
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(su + kOffPh + off), "r"(hi[4 * q4]),
-                                 "r"(hi[4 * q4 + 1]), "r"(hi[4 * q4 + 2]), "r"(hi[4 * q4 + 3])
-                                 : "memory");
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(su + kOffPl + off), "r"(lo[4 * q4]),
-                                 "r"(lo[4 * q4 + 1]), "r"(lo[4 * q4 + 2]), "r"(lo[4 * q4 + 3])
-                                 : "memory");
-                }
+                // keys 32c .. 32c+31: hi in columns 32c .. 32c+15, lo in 32c+16 .. 32c+31
+                tmem_st16(tS + c * 32, hi);
+                tmem_st16(tS + c * 32 + 16, lo);
             }
-            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            tc_fence_before();
-            mbar_arrive(&b.s_empty);
-            // values past the tile's last position: exact zeros (the cache there holds anything)
-            if (j == nb - 1 && k0 + row > p_last) {
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            // values past the CTA's last position: exact zeros (the cache there holds anything)
+            if (j == nb - 1 && k0 + row > p_end) {
                 const uint32_t vrow = su + kOffV + (j & 1) * kTile + row * 128;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
@@ -280,26 +291,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
                     asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + kBox + ch * 16), "r"(0u)
                                  : "memory");
                 }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive(&b.p_full);
-            l = l * alpha + lsum;
-            m = m_new;
-            alpha_prev = alpha;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&b.p_full[t]);
         }
-        fold_o(nb - 1, alpha_prev);
+        // the tile's last P V, then out = bf16(O / l)
+        if (nbt[t] > 0) {
+            if (ok && !*abort && !mbar_wait(&b.o_full[t], (nbt[t] - 1) & 1, a.status)) ok = false;
+            tc_fence_after();
+        }
         pdl_trigger();
         if (!ok) *abort = 1;
-        if (row < nr) {
-            bf16* out = a.out + (size_t)(r0 + row) * a.n_q * kHeadDim + (size_t)h * kHeadDim;
+        if (nbt[t] > 0) {  // every lane loads (whole-warp instruction); rows of the chunk store
+            bf16* out = a.out + (size_t)(r0[t] + row) * a.n_q * kHeadDim + (size_t)h * kHeadDim;
 #pragma unroll
-            for (int c = 0; c < kHeadDim / 8; ++c) {
-                uint4 w;
-                w.x = pack_bf16(rn(o[8 * c + 0] / l), rn(o[8 * c + 1] / l));
-                w.y = pack_bf16(rn(o[8 * c + 2] / l), rn(o[8 * c + 3] / l));
-                w.z = pack_bf16(rn(o[8 * c + 4] / l), rn(o[8 * c + 5] / l));
-                w.w = pack_bf16(rn(o[8 * c + 6] / l), rn(o[8 * c + 7] / l));
-                *reinterpret_cast<uint4*>(out + 8 * c) = w;
+            for (int c = 0; c < kHeadDim / 32; ++c) {
+                float v[32];
+                tmem_ld32(tO + c * 32, v);
+                if (row < nr[t]) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint4 w;
+                        w.x = pack_rn(v[8 * q + 0] / l, v[8 * q + 1] / l);
+                        w.y = pack_rn(v[8 * q + 2] / l, v[8 * q + 3] / l);
+                        w.z = pack_rn(v[8 * q + 4] / l, v[8 * q + 5] / l);
+                        w.w = pack_rn(v[8 * q + 6] / l, v[8 * q + 7] / l);
+                        *reinterpret_cast<uint4*>(out + c * 32 + 8 * q) = w;
+                    }
+                }
             }
         }
     }
@@ -307,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
     // every MMA was waited for by the softmax warps (or the kernel gave up): free TMEM
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 9) {
         if (*abort) __nanosleep(500000);  // let copies and MMAs already issued finish
         tc_fence_after();
         __syncwarp();
@@ -329,7 +350,7 @@ cudaError_t launch_attn_prefill(const AttnPrefillArgs& a, cudaStream_t st, bool 
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t c = {};
-    c.gridDim = dim3(a.n_q, (a.n_rows + kBM - 1) / kBM);
+    c.gridDim = dim3(a.n_q, (a.n_rows + 2 * kBM - 1) / (2 * kBM));
     c.blockDim = dim3(kThreads);
     c.dynamicSmemBytes = kSmem;
     c.stream = st;
