@@ -14,8 +14,9 @@
 //            tensor memory), then O += P V (M = 128 rows, N = 128 dims) with the
 //            weights P read from tensor memory, where the softmax wrote them
 //            over S, and V read MN-major from shared memory.
-// While one tile's rows run their softmax, the tensor cores work on the other
-// tile, and both tiles share each key/value block.
+// Tile B runs half a period behind tile A, so that while one tile's rows run
+// their softmax the tensor cores work on the other tile; both tiles share each
+// key/value block.
 //
 // Softmax of a row over block j: scores s (fp32 dot products of the bf16 q and
 // k), visible keys only (causal), block max b = max(s) log2(e)/sqrt(128).  The
@@ -164,48 +165,58 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN);
             constexpr uint32_t idPV = idesc_bf16_f32_bmn(kBM, kHeadDim);
-            bool ok = mbar_wait(&b.q_full, 0, a.status);
+            // S_t(j) into tile t's score columns (only after P V of block j-1,
+            // which read the weights there, has finished)
+            auto issue_s = [&](int t, int j) {
+                tc_fence_after();
+                const uint32_t kt = su + kOffK + (j & 1) * kTile;
+#pragma unroll
+                for (int kk = 0; kk < kHeadDim / 16; ++kk)
+                    tc_mma_bf16(tmem + t * 128, kdesc(su + kOffQ + t * kTile, kk), kdesc(kt, kk), idS,
+                                kk > 0 ? 1u : 0u);
+                tc_commit(&b.s_full[t]);
+            };
+            // O_t += P_hi V + P_lo V of block j
+            auto issue_pv = [&](int t, int j) {
+                tc_fence_after();
+                const uint32_t vt = su + kOffV + (j & 1) * kTile;
+                const uint32_t tp = tmem + t * 128, to = tmem + 256 + t * 128;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    tc_mma_bf16_ta(to, tp + 32 * (kk >> 1) + 8 * (kk & 1), sdesc_sw128_mn(vt + kk * 2048, kBox), idPV,
+                                   (j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    tc_mma_bf16_ta(to, tp + 32 * (kk >> 1) + 16 + 8 * (kk & 1), sdesc_sw128_mn(vt + kk * 2048, kBox),
+                                   idPV, 1u);
+                tc_commit(&b.o_full[t]);
+            };
+            auto kv_ready = [&](int j) { return mbar_wait(&b.kv_full[j & 1], (j >> 1) & 1, a.status); };
+            // Tile B runs half a period behind tile A: its first scores are issued
+            // once A's first softmax is done, and from then on each tile's P V and
+            // next S fill the tensor cores while the other tile's rows run their
+            // softmax.
+            bool ok = mbar_wait(&b.q_full, 0, a.status) && kv_ready(0);
+            if (ok) issue_s(0, 0);
             for (int j = 0; j < nb && ok; ++j) {
-                const int buf = j & 1;
-                ok = mbar_wait(&b.kv_full[buf], (j >> 1) & 1, a.status);
-                const uint32_t kt = su + kOffK + buf * kTile, vt = su + kOffV + buf * kTile;
-                // S = Q K^T per tile, once that tile's previous P V (which read
-                // the weights in the same columns) has finished
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (!ok || j >= nbt[t]) continue;
-                    if (j > 0 && !mbar_wait(&b.o_full[t], (j - 1) & 1, a.status)) {
-                        ok = false;
-                        continue;
+                if (j < nbt[0]) {
+                    if (!(ok = mbar_wait(&b.p_full[0], j & 1, a.status))) break;
+                    if (j == 0 && nbt[1] > 0) issue_s(1, 0);
+                    issue_pv(0, j);
+                    if (j + 1 < nbt[0]) {
+                        if (!(ok = mbar_wait(&b.o_full[0], j & 1, a.status) && kv_ready(j + 1))) break;
+                        issue_s(0, j + 1);
                     }
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < kHeadDim / 16; ++kk)
-                        tc_mma_bf16(tmem + t * 128, kdesc(su + kOffQ + t * kTile, kk), kdesc(kt, kk), idS,
-                                    kk > 0 ? 1u : 0u);
-                    tc_commit(&b.s_full[t]);
                 }
-                // O += P_hi V + P_lo V per tile once its weights are written
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (!ok || j >= nbt[t]) continue;
-                    if (!mbar_wait(&b.p_full[t], j & 1, a.status)) {
-                        ok = false;
-                        continue;
-                    }
-                    tc_fence_after();
-                    const uint32_t tp = tmem + t * 128, to = tmem + 256 + t * 128;
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        tc_mma_bf16_ta(to, tp + 32 * (kk >> 1) + 8 * (kk & 1), sdesc_sw128_mn(vt + kk * 2048, kBox),
-                                       idPV, (j > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        tc_mma_bf16_ta(to, tp + 32 * (kk >> 1) + 16 + 8 * (kk & 1),
-                                       sdesc_sw128_mn(vt + kk * 2048, kBox), idPV, 1u);
-                    tc_commit(&b.o_full[t]);
+                if (j < nbt[1]) {
+                    if (!(ok = mbar_wait(&b.p_full[1], j & 1, a.status))) break;
+                    issue_pv(1, j);
                 }
-                if (ok) tc_commit(&b.kv_empty[buf]);
+                tc_commit(&b.kv_empty[j & 1]);  // both tiles are done with block j
+                if (j + 1 < nbt[1]) {
+                    if (!(ok = mbar_wait(&b.o_full[1], j & 1, a.status) && kv_ready(j + 1))) break;
+                    issue_s(1, j + 1);
+                }
             }
             if (!ok) *abort = 1;
         }
