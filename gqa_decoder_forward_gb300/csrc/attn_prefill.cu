@@ -237,16 +237,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
             // pass 1: block max of the visible raw scores (the scale is positive)
             float mx = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                float v[32];
-                tmem_ld32(tS + c * 32, v);
+            for (int c = 0; c < kBN / 64; ++c) {
+                float v[64];
+                tmem_ld64(tS + c * 64, v);
                 if (whole) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, v[e]);
+                    for (int e = 0; e < 64; ++e) mx = fmaxf(mx, v[e]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (k0 + c * 32 + e <= pos) mx = fmaxf(mx, v[e]);
+                    for (int e = 0; e < 64; ++e)
+                        if (k0 + c * 64 + e <= pos) mx = fmaxf(mx, v[e]);
                 }
             }
             const float bmax = mx * kScale;
@@ -277,26 +277,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
             // sums over keys 4i+0..3, added in order at the end
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < kBN / 32; ++c) {
-                float v[32];
-                tmem_ld32(tS + c * 32, v);
-                uint32_t hi[16], lo[16];
+            for (int c2 = 0; c2 < kBN / 64; ++c2) {
+                float v[64];
+                tmem_ld64(tS + c2 * 64, v);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float p0 = ex2(fmaf(v[e], kScale, -m)), p1 = ex2(fmaf(v[e + 1], kScale, -m));
-                    if (!whole) {
-                        if (k0 + c * 32 + e > pos) p0 = 0.f;
-                        if (k0 + c * 32 + e + 1 > pos) p1 = 0.f;
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int c = 2 * c2 + h2;  // keys 32c .. 32c+31
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float p0 = ex2(fmaf(v[32 * h2 + e], kScale, -m));
+                        float p1 = ex2(fmaf(v[32 * h2 + e + 1], kScale, -m));
+                        if (!whole) {
+                            if (k0 + c * 32 + e > pos) p0 = 0.f;
+                            if (k0 + c * 32 + e + 1 > pos) p1 = 0.f;
+                        }
+                        ls[e & 3] += p0;
+                        ls[(e + 1) & 3] += p1;
+                        // hi = bf16 truncation of p, lo = bf16 truncation of the exact rest p - hi
+                        hi[e / 2] = pack_trunc(p0, p1);
+                        lo[e / 2] = pack_trunc(p0 - trunc_bf16(p0), p1 - trunc_bf16(p1));
                     }
-                    ls[e & 3] += p0;
-                    ls[(e + 1) & 3] += p1;
-                    // hi = bf16 truncation of p, lo = bf16 truncation of the exact rest p - hi
-                    hi[e / 2] = pack_trunc(p0, p1);
-                    lo[e / 2] = pack_trunc(p0 - trunc_bf16(p0), p1 - trunc_bf16(p1));
+                    // hi in columns 32c .. 32c+15, lo in 32c+16 .. 32c+31
+                    tmem_st16(tS + c * 32, hi);
+                    tmem_st16(tS + c * 32 + 16, lo);
                 }
-                // keys 32c .. 32c+31: hi in columns 32c .. 32c+15, lo in 32c+16 .. 32c+31
-                tmem_st16(tS + c * 32, hi);
-                tmem_st16(tS + c * 32 + 16, lo);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // values past the CTA's last position: exact zeros (the cache there holds anything)
