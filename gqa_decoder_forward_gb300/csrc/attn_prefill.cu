@@ -24,9 +24,9 @@
 // reference becomes b and the running sum l and the tensor-memory output O are
 // multiplied by 2^(m_old - m_new) (exactly the online softmax, rescaled lazily:
 // every weight stays <= 2^8).  Weights p = 2^(s log2(e)/sqrt(128) - m) enter
-// P V as hi = p truncated to bf16 and lo = (p - hi) truncated to bf16
-// (p to within 2^-14 relative; they are not rounded to bf16); l += sum p in a
-// fixed order.  At the end out = bf16(O / l), rounded once.
+// P V as hi = bf16(p) and lo = bf16(p - hi), both rounded to nearest (about
+// 16 significant bits, unbiased; they are not rounded to bf16); l += sum p in
+// a fixed order.  At the end out = bf16(O / l), rounded once.
 //
 // Determinism: a row's arithmetic depends only on the row and its position.
 // Key blocks sit at absolute positions and are visited in order from 0; keys
@@ -70,12 +70,6 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-
-// The bf16 truncations of two floats, packed (a in the low half).
-__device__ __forceinline__ uint32_t pack_trunc(float a, float b) {
-    return __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x7632);
-}
-__device__ __forceinline__ float trunc_bf16(float a) { return __uint_as_float(__float_as_uint(a) & 0xFFFF0000u); }
 
 __device__ __forceinline__ uint32_t pack_rn(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -294,9 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
                         }
                         ls[e & 3] += p0;
                         ls[(e + 1) & 3] += p1;
-                        // hi = bf16 truncation of p, lo = bf16 truncation of the exact rest p - hi
-                        hi[e / 2] = pack_trunc(p0, p1);
-                        lo[e / 2] = pack_trunc(p0 - trunc_bf16(p0), p1 - trunc_bf16(p1));
+                        // hi = bf16(p), lo = bf16(p - hi), both rounded to nearest (unbiased)
+                        const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+                        hi[e / 2] = *reinterpret_cast<const uint32_t*>(&hh);
+                        lo[e / 2] = pack_rn(p0 - __low2float(hh), p1 - __high2float(hh));
                     }
                     // hi in columns 32c .. 32c+15, lo in 32c+16 .. 32c+31
                     tmem_st16(tS + c * 32, hi);

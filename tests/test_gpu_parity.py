@@ -566,3 +566,64 @@ def test_resume_from_prefix_store_equals_fresh(tiny):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16)), t
     with pytest.raises(tfl.TflError):
         tfl.tfl_kv_copy_prefix(m, stored, resumed, 301)   # beyond length(src)
+
+
+# ---- prompt attention: odd chunk shapes ----------------------------------------------
+
+PATTN_CASES = [(0, 1), (0, 2), (0, 128), (0, 129), (0, 255), (0, 256), (0, 257), (5, 127), (127, 1), (127, 130),
+               (300, 200), (383, 384), (640, 300)]
+
+
+@pytest.fixture(scope="module")
+def pattn_tiny(tiny):
+    w, _ = tiny
+    m = _tiny_model(w, max_rows=512, max_context=1024)
+    kv = m.kv(1024)
+    K = synth.normal_bf16(81, 0, (1024, TINY.n_kv, 128), 1.0, "cuda")
+    V = synth.normal_bf16(82, 0, (1024, TINY.n_kv, 128), 1.0, "cuda")
+    kv.write(0, 0, K, V)
+    return m, kv, synth.bits(K), synth.bits(V)
+
+
+@pytest.mark.parametrize("pos0,rows", PATTN_CASES)
+def test_prompt_attention_chunk_shapes_tiny(orc, pattn_tiny, pos0, rows):
+    """The prompt attention (two 128-row tiles per CTA; tile B empty, partial or
+    one key block ahead of tile A) on chunks of odd sizes at odd positions, against
+    the oracle's attention over the same cached keys and values."""
+    m, kv, Kb, Vb = pattn_tiny
+    q = synth.normal_bf16(83, pos0 * 1000 + rows, (rows, TINY.n_q * 128), 1.0, "cuda")
+    out = torch.empty_like(q)
+    tfl.tfl_layer_op(m, "attention", 0, q, out, kv=kv, pos0=pos0, prompt=True)
+    n = pos0 + rows
+    qb = synth.bits(q).reshape(rows, TINY.n_q, 128)
+    ref = orc.attention(qb, np.arange(pos0, n, dtype=np.int32), Kb[:n], Vb[:n])
+    # gate: 1 ulp of the output plus, times sum_t p_t |v_t| (computed in double),
+    # the fp32 accumulation allowance sqrt(keys) 2^-24 and the representation
+    # error of the weights as bf16 hi + lo, |p - hi - lo| <= 2^-18 p
+    qf, Kf, Vf = gu.bf16_to_f64(qb), gu.bf16_to_f64(Kb[:n, 0]), gu.bf16_to_f64(Vb[:n, 0])
+    absum = np.empty((rows, TINY.n_q, 128))
+    for r in range(rows):
+        k = pos0 + r + 1
+        s = qf[r] @ Kf[:k].T / np.sqrt(128.0)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        absum[r] = (p / p.sum(axis=1, keepdims=True)) @ np.abs(Vf[:k])
+    keys = np.arange(pos0 + 1, n + 1, dtype=np.float64)[:, None, None]
+    bound = gu.ulp_of(ref).reshape(rows, TINY.n_q, 128) + (np.sqrt(keys) * 2.0 ** -24 + 2.0 ** -18) * absum
+    gu.assert_bound_gate(synth.bits(out).reshape(rows, TINY.n_q, 128), ref.reshape(rows, TINY.n_q, 128), bound,
+                         f"prompt attention pos0 {pos0} rows {rows}")
+
+
+def test_prompt_attention_rows_independent_of_chunking(pattn_tiny):
+    """Rows 0..383 in one call equal the same rows in calls of 100, 1 and 283."""
+    m, kv, _, _ = pattn_tiny
+    q = synth.normal_bf16(84, 0, (384, TINY.n_q * 128), 1.0, "cuda")
+    whole = torch.empty_like(q)
+    tfl.tfl_layer_op(m, "attention", 0, q, whole, kv=kv, pos0=0, prompt=True)
+    parts = torch.empty_like(q)
+    r0 = 0
+    for n in (100, 1, 283):
+        o = torch.empty((n, q.shape[1]), dtype=torch.bfloat16, device="cuda")
+        tfl.tfl_layer_op(m, "attention", 0, q[r0:r0 + n].contiguous(), o, kv=kv, pos0=r0, prompt=True)
+        parts[r0:r0 + n] = o
+        r0 += n
+    assert torch.equal(whole.view(torch.int16), parts.view(torch.int16))
