@@ -3,13 +3,15 @@
 // and the chunk's own earlier rows on the tensor units), one pass with an
 // online softmax, the products on the 5th-generation tensor cores.
 //
-// One CTA per (query head h, pair of 128-row tiles A and B), 320 threads:
-//   warps 0-3 softmax of tile A, warps 4-7 softmax of tile B: one query row
-//            per thread (tensor-memory lane = row of the tile);
-//   warp 8   TMA producer: both tiles' queries once, then the keys and values
+// One CTA per (query head h, pair of 128-row tiles A and B), 576 threads:
+//   warps 0-7 softmax of tile A, warps 8-15 softmax of tile B: two threads per
+//            query row (tensor-memory lane = row of the tile), each over half
+//            the keys of a block and half the output dims, the row max and
+//            sum exchanged through shared memory;
+//   warp 16  TMA producer: both tiles' queries once, then the keys and values
 //            of KV head h / G block by block (a block = 128 positions = one
 //            cache page), double-buffered;
-//   warp 9   allocates tensor memory and issues the MMAs (one thread), per
+//   warp 17  allocates tensor memory and issues the MMAs (one thread), per
 //            block and tile: S = Q K^T (M = 128 rows, N = 128 keys, fp32 in
 //            tensor memory), then O += P V (M = 128 rows, N = 128 dims) with the
 //            weights P read from tensor memory, where the softmax wrote them
@@ -42,7 +44,7 @@
 namespace tfl {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 576;
 constexpr int kBM = 128;                  // query rows per tile
 constexpr int kBN = kPage;                // keys per block: one cache page
 constexpr int kBox = 128 * 64 * 2;        // 16 KB: 128 rows x 64 columns, 128-byte swizzle
@@ -51,9 +53,13 @@ constexpr int kTmemCols = 512;            // S/P of A, S/P of B, O of A, O of B:
 constexpr float kScale = 0.12751743074640502f;  // log2(e) / sqrt(128)
 constexpr float kRescale = 8.f;           // lazy rescale threshold (log2 units)
 
-// Shared memory (from a 1024-byte aligned base): Q[2], K[2], V[2], barriers.
+constexpr int kProducerWarp = 16, kMmaWarp = 17;
+
+// Shared memory (from a 1024-byte aligned base): Q[2], K[2], V[2], the row-max
+// exchange ([tile][block parity][half][row]) and row-sum exchange ([tile][half][row]), barriers.
 constexpr int kOffQ = 0, kOffK = 2 * kTile, kOffV = 4 * kTile;
-constexpr int kOffBar = 6 * kTile;
+constexpr int kOffX = 6 * kTile;
+constexpr int kOffBar = kOffX + (2 * 2 * 2 * 128 + 2 * 2 * 128) * 4;
 constexpr int kSmem = 1024 + kOffBar + 16 * 8;
 
 struct Bars {
@@ -111,13 +117,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
             mbar_init(&b.kv_full[i], 1);
             mbar_init(&b.kv_empty[i], 1);
             mbar_init(&b.s_full[i], 1);
-            mbar_init(&b.p_full[i], kBM);
+            mbar_init(&b.p_full[i], 2 * kBM);
             mbar_init(&b.o_full[i], 1);
         }
         b.abort = 0;
         mbar_init_fence();
     }
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&b.tmem, kTmemCols);
         tmem_relinquish();
     }
@@ -127,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
     const uint32_t tmem = b.tmem;
     pdl_wait();
 
-    if (warp == 8) {
+    if (warp == kProducerWarp) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const uint64_t keep = policy_evict_last(), once = policy_evict_first();
@@ -154,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
                 }
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN);
@@ -215,34 +221,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
             if (!ok) *abort = 1;
         }
     } else {
-        // ---------------- softmax: one row per thread ----------------
-        const int t = warp >> 2;
+        // ---------------- softmax: two threads per row ----------------
+        // warps 8t .. 8t+7 serve tile t; warp w covers tensor-memory lanes
+        // 32 (w mod 4) .. +31 (the rows) and half (w / 4) mod 2 of the columns
+        // (keys 64 hf .. 64 hf + 63 of S, dims 64 hf .. of O)
+        const int t = warp >> 3, hf = (warp >> 2) & 1;
         const int row = (warp & 3) * 32 + lane;
         const int pos = min(p_first[t] + row, p_last[t]);  // rows past the chunk see only real keys
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_off + t * 128, tO = tmem + lane_off + 256 + t * 128;
+        const uint32_t tS = tmem + lane_off + t * 128, tO = tmem + lane_off + 256 + t * 128 + hf * 64;
+        float* xm = reinterpret_cast<float*>(base + kOffX) + t * (2 * 2 * kBM);  // [block parity][half][row]
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nbt[t]; ++j) {
             if (ok && !*abort && !mbar_wait(&b.s_full[t], j & 1, a.status)) ok = false;
             tc_fence_after();
-            const int k0 = j * kBN;
-            const bool whole = k0 + kBN - 1 <= pos;  // every key of the block is visible to the row
-            // pass 1: block max of the visible raw scores (the scale is positive)
+            const int k0 = j * kBN, kh = k0 + hf * 64;  // first key of this thread's half
+            const bool whole = k0 + kBN - 1 <= pos;      // every key of the block is visible to the row
+            // pass 1: max of the visible raw scores of this half, then of the row
             float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < kBN / 64; ++c) {
+            {
                 float v[64];
-                tmem_ld64(tS + c * 64, v);
+                tmem_ld64(tS + hf * 64, v);
                 if (whole) {
 #pragma unroll
                     for (int e = 0; e < 64; ++e) mx = fmaxf(mx, v[e]);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 64; ++e)
-                        if (k0 + c * 64 + e <= pos) mx = fmaxf(mx, v[e]);
+                        if (kh + e <= pos) mx = fmaxf(mx, v[e]);
                 }
             }
+            float* xj = xm + (j & 1) * (2 * kBM);
+            xj[hf * kBM + row] = mx;
+            named_barrier(1 + t, 8 * 32);
+            mx = fmaxf(xj[row], xj[kBM + row]);
             const float bmax = mx * kScale;
             const bool rescale = bmax > m + kRescale;  // a new reference max (always on block 0)
             const float alpha = rescale ? ex2(m - bmax) : 1.f;
@@ -251,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
             // rows that keep their reference rewrite O times 1
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-                for (int c = 0; c < kHeadDim / 32; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     float v[32];
                     tmem_ld32(tO + c * 32, v);
                     uint32_t w[16];
@@ -267,40 +280,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
                 l *= alpha;
                 m = bmax;
             }
-            // pass 2: weights (hi, lo) written over the scores; four running
-            // sums over keys 4i+0..3, added in order at the end
+            // pass 2: this half's weights (hi, lo) written over its scores; four
+            // running sums over keys 4i+0..3, added in order at the end
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c2 = 0; c2 < kBN / 64; ++c2) {
-                float v[64];
-                tmem_ld64(tS + c2 * 64, v);
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int c = 2 * hf + h2;  // keys 32c .. 32c+31 of the block
+                float v[32];
+                tmem_ld32(tS + c * 32, v);
+                uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int c = 2 * c2 + h2;  // keys 32c .. 32c+31
-                    uint32_t hi[16], lo[16];
-#pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        float p0 = ex2(fmaf(v[32 * h2 + e], kScale, -m));
-                        float p1 = ex2(fmaf(v[32 * h2 + e + 1], kScale, -m));
-                        if (!whole) {
-                            if (k0 + c * 32 + e > pos) p0 = 0.f;
-                            if (k0 + c * 32 + e + 1 > pos) p1 = 0.f;
-                        }
-                        ls[e & 3] += p0;
-                        ls[(e + 1) & 3] += p1;
-                        // hi = bf16(p), lo = bf16(p - hi), both rounded to nearest (unbiased)
-                        const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
-                        hi[e / 2] = *reinterpret_cast<const uint32_t*>(&hh);
-                        lo[e / 2] = pack_rn(p0 - __low2float(hh), p1 - __high2float(hh));
+                for (int e = 0; e < 32; e += 2) {
+                    float p0 = ex2(fmaf(v[e], kScale, -m));
+                    float p1 = ex2(fmaf(v[e + 1], kScale, -m));
+                    if (!whole) {
+                        if (k0 + c * 32 + e > pos) p0 = 0.f;
+                        if (k0 + c * 32 + e + 1 > pos) p1 = 0.f;
                     }
-                    // hi in columns 32c .. 32c+15, lo in 32c+16 .. 32c+31
-                    tmem_st16(tS + c * 32, hi);
-                    tmem_st16(tS + c * 32 + 16, lo);
+                    ls[e & 3] += p0;
+                    ls[(e + 1) & 3] += p1;
+                    // hi = bf16(p), lo = bf16(p - hi), both rounded to nearest (unbiased)
+                    const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
+                    hi[e / 2] = *reinterpret_cast<const uint32_t*>(&hh);
+                    lo[e / 2] = pack_rn(p0 - __low2float(hh), p1 - __high2float(hh));
                 }
+                // hi in columns 32c .. 32c+15, lo in 32c+16 .. 32c+31
+                tmem_st16(tS + c * 32, hi);
+                tmem_st16(tS + c * 32 + 16, lo);
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);  // this half's running sum
             // values past the CTA's last position: exact zeros (the cache there holds anything)
-            if (j == nb - 1 && k0 + row > p_end) {
+            if (hf == 0 && j == nb - 1 && k0 + row > p_end) {
                 const uint32_t vrow = su + kOffV + (j & 1) * kTile + row * 128;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
@@ -314,7 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
             tc_fence_before();
             mbar_arrive(&b.p_full[t]);
         }
-        // the tile's last P V, then out = bf16(O / l)
+        // the row's sum = first half's + second half's
+        float* xl = reinterpret_cast<float*>(base + kOffX) + 2 * (2 * 2 * kBM) + t * (2 * kBM);
+        xl[hf * kBM + row] = l;
+        named_barrier(1 + t, 8 * 32);
+        l = xl[row] + xl[kBM + row];
+        // the tile's last P V, then out = bf16(O / l) for this half's 64 dims
         if (nbt[t] > 0) {
             if (ok && !*abort && !mbar_wait(&b.o_full[t], (nbt[t] - 1) & 1, a.status)) ok = false;
             tc_fence_after();
@@ -322,9 +337,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
         pdl_trigger();
         if (!ok) *abort = 1;
         if (nbt[t] > 0) {  // every lane loads (whole-warp instruction); rows of the chunk store
-            bf16* out = a.out + (size_t)(r0[t] + row) * a.n_q * kHeadDim + (size_t)h * kHeadDim;
+            bf16* out = a.out + (size_t)(r0[t] + row) * a.n_q * kHeadDim + (size_t)h * kHeadDim + hf * 64;
 #pragma unroll
-            for (int c = 0; c < kHeadDim / 32; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 float v[32];
                 tmem_ld32(tO + c * 32, v);
                 if (row < nr[t]) {
@@ -345,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
     // every MMA was waited for by the softmax warps (or the kernel gave up): free TMEM
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         if (*abort) __nanosleep(500000);  // let copies and MMAs already issued finish
         tc_fence_after();
         __syncwarp();
