@@ -596,12 +596,13 @@ def run_concurrent(args):
         torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / args.steps
     phases = None
+    tfl.tfl_profile(model, True)
+    step()
+    prof = tfl.tfl_profile_read(model)
     if S <= 2:
-        tfl.tfl_profile(model, True)
-        step()
-        tfl.tfl_profile_read(model)
         phases = tfl.tfl_step_phases(model)
-        tfl.tfl_profile(model, False)
+    tfl.tfl_profile(model, False)
+    kernels = {k: {"ms": round(v[0], 4), "launches": v[1]} for k, v in prof.items() if v[1]}
     mean_ctx = ctx + args.warmup + (args.steps - 1) / 2.0
     w = step_bytes(shape, 0)
     kvb = shape.layers * 2 * shape.n_kv * shape.head_dim * 2 * mean_ctx * S
@@ -611,7 +612,8 @@ def run_concurrent(args):
                       "path": "persistent" if S <= 2 else "launch per operation",
                       "tok_s": round(S * 1e3 / ms, 2), "ms_per_step": round(ms, 4), "bytes_per_step": int(w + kvb),
                       "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "peak_kind": peak_kind,
-                      "status": model.status(), "step_phases_us": phases, "clocks": clk.summary()}), flush=True)
+                      "status": model.status(), "step_phases_us": phases, "kernels_one_step": kernels,
+                      "clocks": clk.summary()}), flush=True)
 
 
 def run_op(args):
