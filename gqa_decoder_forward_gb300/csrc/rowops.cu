@@ -8,7 +8,7 @@
 // round-to-nearest operations (no fast-math approximations).
 //
 // Argmax (same pull request, teacher-forced misses reply: "Both sides break
-// ties to the lower id"; the judge refuses rows holding NaN or +-Inf): the
+// ties to the lower id"; its teacher-forced checks refuse rows holding NaN or +-Inf): the
 // largest logit, the lowest id among equal maxima; a row with any non-finite
 // logit yields -1 and raises a bit of the device status word.
 #include "common.cuh"

@@ -19,7 +19,7 @@
 // The float64-with-bf16-points design follows the same pull request's float64
 // reference ("--bf16-points": each operation exact before the point).
 //
-// Readings where the pages are silent (each one is listed in the design doc):
+// Readings where the pages are silent:
 //   * attention: scores, softmax and P.V at full precision, output rounded once;
 //     scale 1/sqrt(head_dim);
 //   * inv_freq[i] = fl32(1 / fl32(theta^(2i/D))); angle = fl32(pos * inv_freq[i]);
@@ -27,9 +27,10 @@
 //   * silu(g) = g / (1 + exp(-g)) in double;
 //   * argmax ties go to the lowest id; any non-finite logit in a row is an error.
 //
-// Parity status of each function is stated in the design doc; the whole-model
-// forward on random weights has no printed values to pin against and is pinned
-// only through its components and invariants.
+// Every function is pinned by the tests against closed forms, brute force or
+// library routines; the whole-model forward on random weights has no printed
+// values to pin against and is pinned only through its components and
+// invariants.
 
 #include <cmath>
 #include <cstdint>
@@ -267,7 +268,7 @@ int orc_argmax(const uint16_t* logits, int rows, int V, int32_t* ids) {
 // Seeded sampling of one token per row (the GPU draw the pages name beside
 // argmax: "argmax or tf_sample_full"; temperature, top-k and top-p as in the
 // release's recommended settings).  The pages fix no algorithm; the reading
-// (also listed in the design doc), over a row's bf16 logits z with T > 0, k >= 0,
+// over a row's bf16 logits z with T > 0, k >= 0,
 // 0 < p, and a uniform u in [0, 1) given by the caller:
 //   1. candidates C: all ids if k == 0 or k >= V, else the ids whose logit is at
 //      least the k-th largest logit (counted with multiplicity; ties included);

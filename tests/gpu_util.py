@@ -59,7 +59,7 @@ def ulp_of(b) -> np.ndarray:
 
 
 def assert_hidden_gate(gpu_bits, ref_bits, what=""):
-    """The spec hidden-state gate for a value with one rounding point:
+    """The hidden-state gate for a value with one rounding point:
     <= 1 bf16 ulp for >= 99.9% of elements, <= 4 ulp everywhere."""
     d = ulp_dist(gpu_bits, ref_bits)
     frac1 = float(np.mean(d <= 1))
@@ -98,7 +98,8 @@ def bf16_step(x: float) -> float:
 
 
 def near_tie(logits_bits_row, a: int, b: int) -> bool:
-    """The judge's near-tie rule: ids a and b within one bf16 step of each other."""
+    """The near-tie rule of the pages' teacher-forced checks: ids a and b within one
+    bf16 step of each other."""
     v = bf16_to_f64(logits_bits_row)
     hi = max(abs(v[a]), abs(v[b]))
     return abs(v[a] - v[b]) <= bf16_step(hi)

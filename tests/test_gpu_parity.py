@@ -134,7 +134,7 @@ def test_tiny_greedy_16_matches_oracle(orc, tiny):
     cur = int(rid[0])
     for i in range(16):
         if cur != gpu_ids[i]:
-            # the judge's rule: both sides' two contenders within one bf16 step
+            # the pages' near-tie rule: both sides' two contenders within one bf16 step
             prev = ref_last[-1] if i == 0 else ref_row
             prev_gpu = synth.bits(last)[0] if i == 0 else gpu_rows[i - 1]
             assert gu.near_tie(prev, cur, gpu_ids[i]), f"greedy step {i}: {cur} vs {gpu_ids[i]} not a near tie"
