@@ -936,6 +936,8 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
     cudaError_t ce = cudaMemcpy(m->cos_t, c.data(), c.size() * 2, cudaMemcpyHostToDevice);
     if (ce == cudaSuccess) ce = cudaMemcpy(m->sin_t, s.data(), s.size() * 2, cudaMemcpyHostToDevice);
     if (ce == cudaSuccess) ce = cudaMemset(m->status, 0, 256);
+    // sampling counts start at zero; every tfl_sample call leaves them zero again
+    if (ce == cudaSuccess) ce = cudaMemset(m->scounts, 0, (size_t)cfg->max_decode_rows * 65536 * 4);
     if (ce != cudaSuccess) {
         delete m;
         return fail(TFL_E_CUDA, "uploading the RoPE table failed: %s", cudaGetErrorString(ce));
