@@ -114,3 +114,26 @@ def test_sample_arguments_are_checked(tiny_model):
         with pytest.raises(tfl.TflError) as e:
             tiny_model.sample(logits, T, k, p, u, ids)
         assert e.value.code == tfl.TFL_E_ARG
+
+
+def test_sample_scratch_cycle(orc, big_model):
+    """The draw keeps per-value counts in the model's scratch and leaves them zero
+    after every call: calls of different row counts and contents in sequence,
+    with non-finite rows between them, each equal the oracle."""
+    seq = [(16, 80, 1.5, (0.6, 20, 0.95)), (3, 81, 3.0, (1.0, 0, 0.9)), (5, 82, 0.5, (0.7, 50, 1.0)),
+           (16, 83, 2.0, (0.9, 0, 0.5))]
+    for i, (rows, seed, std, (T, k, p)) in enumerate(seq):
+        logits = synth.normal_bf16(seed, 1, (rows, L1.vocab), std, "cuda")
+        if i == 2:
+            logits[1, 1000] = float("inf")
+            logits[4, 7] = float("nan")
+        u = _uniforms(seed + 1, rows)
+        got, st = _run(big_model, logits, T, k, p, u)
+        ref, _ = orc.sample(synth.bits(logits), T, k, p, u.double().numpy())
+        if i == 2:
+            assert st == tfl.TFL_E_NONFINITE and got[1] == -1 and got[4] == -1
+            keep = [0, 2, 3]
+            assert np.array_equal(got[keep], ref[keep]), (i, got, ref)
+        else:
+            assert st == tfl.TFL_OK
+            assert np.array_equal(got, ref), (i, np.nonzero(got != ref))
