@@ -13,6 +13,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "attn_decode.cuh"
 #include "common.cuh"
 #include "../../include/tfl.h"
 
@@ -364,7 +365,8 @@ cudaError_t mv_launch(tfl_model* m, const MatvecArgs& e, const CUtensorMap* w0, 
 
 // The layer stack over n rows described by rm (decode kernels).  Input: ids
 // (embedding gather) or h_in; output: the residual stream in m->h.
-int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h_in, cudaStream_t st) {
+int run_layers(tfl_model* m, const RowMap& rm, const KvMaps& maps, const int32_t* ids, const void* h_in,
+               cudaStream_t st) {
     const tfl_config& c = m->cfg;
     const int n = rm.n_rows, H = c.hidden, qd = c.n_q * kHeadDim;
     const bool pdl = m->pdl && st != nullptr;  // no programmatic launch on the legacy stream
@@ -414,7 +416,7 @@ int run_layers(tfl_model* m, const RowMap& rm, const int32_t* ids, const void* h
         at.n_kv = c.n_kv;
         at.layer = l;
         at.rows = rm;
-        LAUNCH(m, K_ATTN, st, launch_attn_block(at, st, pdl));
+        LAUNCH(m, K_ATTN, st, launch_attn_block_tma(at, maps, m->status, st, pdl));
         LAUNCH(m, K_MERGE, st, launch_attn_merge(at, st, pdl));
 
         MatvecArgs o = {};
@@ -572,7 +574,9 @@ int decode_common(tfl_model* m, tfl_kv* const* kvs, int n_streams, const int* ro
         for (int s = 0; s < n_streams; ++s) kvs[s]->length += rows[s];
         return ok();
     }
-    e = run_layers(m, rm, ids, h_in, st);
+    KvMaps maps;
+    for (int s = 0; s < n_streams; ++s) maps.m[s] = kvs[s]->kvmap;
+    e = run_layers(m, rm, maps, ids, h_in, st);
     if (e) return e;
     if (h_out) CK(cudaMemcpyAsync(h_out, m->h, (size_t)rm.n_rows * m->cfg.hidden * 2, cudaMemcpyDeviceToDevice, st));
     if (logits) {
@@ -843,6 +847,7 @@ int tfl_init(const tfl_config* cfg, const tfl_weights* w, void* workspace, size_
                 return fail(TFL_E_ARG, "layer %d weight %d NULL or not 16-byte aligned", l, k);
     }
     CK(init_attn_decode());
+    CK(init_attn_decode_tma());
 
     tfl_model* m = new tfl_model();
     m->cfg = *cfg;
@@ -1218,7 +1223,9 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
                 if (e) return e;
                 break;
             }
-            LAUNCH(m, K_ATTN, st, launch_attn_block(at, st, false));
+            KvMaps maps;
+            maps.m[0] = kv->kvmap;
+            LAUNCH(m, K_ATTN, st, launch_attn_block_tma(at, maps, m->status, st, false));
             LAUNCH(m, K_MERGE, st, launch_attn_merge(at, st, false));
             break;
         }

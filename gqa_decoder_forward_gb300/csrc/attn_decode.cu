@@ -12,6 +12,12 @@
 // own online softmax (S = Q K^T, running max, O += P V), the warp partials are
 // combined at the end.  Per (row, head) the CTA writes the unit's max score
 // m_u, sum l_u = sum exp(s - m_u) and o_u = sum exp(s - m_u) v (attn_core.cuh).
+// attn_block_tma_kernel computes the same partials with at most one persistent
+// CTA per SM walking the (unit, KV head, row group) items in a fixed stride: a
+// producer warp streams each item's sub-blocks as 16 KB TMA boxes (keys or
+// values, 64 dims, 128-byte swizzle) through an 8-stage ring, each warp
+// releases a stage once it has read its keys there, and the next item's
+// queries are copied while the warp partials combine.
 // Pass 2 (attn_merge_kernel): per (row, head), M = max_u m_u, then
 // L = sum_u l_u e^(m_u - M) and O = sum_u o_u e^(m_u - M) in unit order,
 // out = bf16(O / L).
@@ -28,8 +34,11 @@
 // in shared memory, and each output element of an mma depends only on its own
 // row of P.  A row gives the same bits alone or beside other rows (one-row
 // steps == windows, solo == batched).
+#include <algorithm>
+
 #include "common.cuh"
 #include "attn_core.cuh"
+#include "attn_decode.cuh"
 #include "tma.cuh"
 #include "warp_mma.cuh"
 
@@ -184,6 +193,247 @@ __global__ void __launch_bounds__(kThreads, 1) attn_block_kernel(const __grid_co
     attn::unit_partial<G>(a, ug, smem_u32(sm.q), sm.comb, src, [] { __syncthreads(); });
 }
 
+// ---- TMA-fed variant -------------------------------------------------------------
+
+constexpr int kTConsumerWarps = 8;
+constexpr int kTThreads = (kTConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kTDepth = 8;                             // ring stages
+constexpr int kTStage = kSub * 64 * 2;                 // 16 KB: 128 positions x 64 dims
+constexpr int kTOffQ = kTDepth * kTStage;              // two query buffers (4 KB each)
+constexpr int kTOffComb = kTOffQ + 2 * attn::kPairs * kHeadDim * 2;
+constexpr int kTOffBar = kTOffComb + attn::kCombFloats * 4;
+constexpr int kTSmem = 1024 + kTOffBar + (2 * kTDepth + 2) * 8;
+static_assert(kSub == kPage, "a sub-block is one cache page");
+static_assert(kTSmem <= 227 * 1024, "shared memory");
+
+// A work item: unit u of KV head g for the group of rows r0 .. r0+nr-1 of stream s.
+struct Item {
+    int s, r0, nr, u, g, k0, nsub, p_first, p_last;
+};
+
+// Item w of the (group, KV head, unit) space, unit fastest; false when the unit
+// holds no key any row of the group sees.
+__device__ __forceinline__ bool item_at(const AttnDecodeArgs& a, int w, int nblk, Item& it) {
+    it.u = w % nblk;
+    const int rest = w / nblk;
+    it.g = rest % a.n_kv;
+    if (!find_group(a.rows, rest / a.n_kv, it.s, it.r0, it.nr)) return false;
+    it.p_first = a.rows.pos0[it.s] + (it.r0 - a.rows.row_start[it.s]);
+    it.p_last = it.p_first + it.nr - 1;
+    it.k0 = it.u * kUnit;
+    if (it.k0 > it.p_last) return false;
+    it.nsub = min(4, (it.p_last - it.k0) / kSub + 1);
+    return true;
+}
+
+// The first item at or after w (in steps of the grid) holding keys; W if none.
+__device__ __forceinline__ int next_item(const AttnDecodeArgs& a, int w, int W, int nblk, Item& it) {
+    for (; w < W; w += gridDim.x)
+        if (item_at(a, w, nblk, it)) return w;
+    return W;
+}
+
+struct TRing {
+    int stage;
+    uint32_t phase;
+    __device__ __forceinline__ void advance() {
+        if (++stage == kTDepth) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// Query (row, head) pair p of item it, 16-byte chunk c.
+template <int G>
+__device__ __forceinline__ const bf16* q_chunk(const AttnDecodeArgs& a, const Item& it, int p, int c) {
+    const int row = it.r0 + p / G, head = it.g * G + p % G;
+    return a.q + (size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + c * 8;
+}
+
+// Sub-block source over the ring (see attn::unit_partial): sub-block j of the
+// item is the four stages after the item's first (K dims 0-63, K 64-127, V
+// 0-63, V 64-127).  After the last sub-block, the next item's queries are
+// copied (cp.async, one 16-byte chunk per consumer thread) into the other
+// query buffer.
+template <int G>
+struct TmaSrc {
+    unsigned char* base;
+    uint64_t *full, *empty;
+    TRing first;  // the item's first stage
+    int* status;
+    volatile int* abort;
+    int k0, p_last, nsub;
+    int stage[4];
+    uint32_t sa[4];
+    const AttnDecodeArgs* a;
+    const Item* nx;  // null: no next item
+    bf16* nq;        // the next item's query buffer
+    __device__ __forceinline__ TRing at(int i) const {
+        TRing r;
+        const int t = first.stage + i;
+        r.stage = t % kTDepth;
+        r.phase = first.phase ^ (uint32_t)((t / kTDepth) & 1);
+        return r;
+    }
+    __device__ __forceinline__ static uint32_t tile(uint32_t lo, uint32_t hi, int row, int col) {
+        return (col < 64 ? lo : hi) + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4);
+    }
+    __device__ __forceinline__ uint32_t k(int, int row, int col) const { return tile(sa[0], sa[1], row, col); }
+    __device__ __forceinline__ uint32_t v(int, int row, int col) const { return tile(sa[2], sa[3], row, col); }
+    // this warp's key rows 16w..16w+15: values past the last visible key become
+    // exact zeros (their weight is 0, and the cache there holds anything)
+    __device__ __forceinline__ void wait(int j) {
+        for (int i = 0; i < 4; ++i) {
+            const TRing r = at(4 * j + i);
+            stage[i] = r.stage;
+            sa[i] = smem_u32(base + r.stage * kTStage);
+            if (!*abort && !mbar_wait(&full[r.stage], r.phase, status)) *abort = 1;
+        }
+        const int nv = min(kSub, p_last + 1 - (k0 + j * kSub));
+        const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int r0 = max(nv, w * 16), r1 = w * 16 + 16;
+        if (r0 < r1) {
+            for (int i = lane; i < (r1 - r0) * 8 * 2; i += 32) {
+                const int half = i >= (r1 - r0) * 8;
+                const int c = half ? i - (r1 - r0) * 8 : i;
+                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"((half ? sa[3] : sa[2]) + r0 * 128 + c * 16),
+                             "r"(0u)
+                             : "memory");
+            }
+            // the stage is refilled by TMA later: order these generic writes before it
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+        }
+    }
+    __device__ __forceinline__ void done(int j) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0)
+            for (int i = 0; i < 4; ++i) mbar_arrive(&empty[stage[i]]);
+        if (j == nsub - 1 && nx) {
+            const int p = threadIdx.x >> 4, c = threadIdx.x & 15, P = nx->nr * G;
+            cp_async16_zfill(&nq[swz(p, c * 8)], p < P ? q_chunk<G>(*a, *nx, p, c) : a->q, p < P);
+            cp_async_commit();
+        }
+    }
+};
+
+struct TConsumerBar {
+    __device__ __forceinline__ void operator()() const { named_barrier(1, kTConsumerWarps * 32); }
+};
+
+template <int G>
+__global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __grid_constant__ AttnDecodeArgs a,
+                                                                      const __grid_constant__ KvMaps maps, int nblk,
+                                                                      int W, int* status) {
+    static_assert(attn::kPairs * 16 == kTConsumerWarps * 32, "one query chunk per consumer thread");
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + kTOffBar);
+    uint64_t* empty = full + kTDepth;
+    volatile int* abort = reinterpret_cast<volatile int*>(empty + kTDepth);
+    bf16* qbuf = reinterpret_cast<bf16*>(base + kTOffQ);
+    float* comb = reinterpret_cast<float*>(base + kTOffComb);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    Item it;
+    const int w0 = next_item(a, blockIdx.x, W, nblk, it);
+    if (w0 >= W) return;  // uniform: no item for this CTA
+    if (tid == 0) {
+        for (int i = 0; i < kTDepth; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kTConsumerWarps);
+        }
+        *abort = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (warp == kTConsumerWarps) {
+        // ---- producer: every item's sub-blocks in the consumers' order ----
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            TRing rp{0, 0u};
+            bool waited = false;
+            for (int w = w0; w < W && !*abort; w = next_item(a, w + gridDim.x, W, nblk, it)) {
+                // an item whose keys all precede the stream's first row of this
+                // call holds cache rows written by earlier calls (every kernel of
+                // the library signals its dependents only after its own
+                // dependency wait): it streams in while the previous kernel ends
+                if (!waited && it.k0 + it.nsub * kSub > a.rows.pos0[it.s]) {
+                    pdl_wait();
+                    waited = true;
+                }
+                const KvView& kv = a.rows.kv[it.s];
+                for (int j = 0; j < it.nsub && !*abort; ++j) {
+                    const int page = __ldg(kv.table + it.k0 / kPage + j);
+                    for (int part = 0; part < 4; ++part) {  // K dims 0-63, K 64-127, V 0-63, V 64-127
+                        if (!mbar_wait(&empty[rp.stage], rp.phase ^ 1u, status)) {
+                            *abort = 1;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[rp.stage], kTStage);
+                        const int row0 = ((a.layer * 2 + (part >> 1)) * kv.n_pages + page) * kPage;
+                        tma_load_3d(base + rp.stage * kTStage, &maps.m[it.s], (part & 1) * 64, it.g, row0,
+                                    &full[rp.stage], pol);
+                        rp.advance();
+                    }
+                }
+            }
+        }
+    } else {
+        // ---- consumers: the eight warps of attn::unit_partial ----
+        pdl_wait();
+        pdl_trigger();
+        for (int i = tid; i < attn::kPairs * 16; i += kTConsumerWarps * 32) {  // the first item's queries
+            const int p = i >> 4, c = i & 15;
+            uint4 val = make_uint4(0u, 0u, 0u, 0u);
+            if (p < it.nr * G) val = *reinterpret_cast<const uint4*>(q_chunk<G>(a, it, p, c));
+            *reinterpret_cast<uint4*>(&qbuf[swz(p, c * 8)]) = val;
+        }
+        TConsumerBar bar;
+        bar();
+        TRing first{0, 0u};
+        int w = w0, qb = 0;
+        while (!*abort) {
+            Item nx;
+            const int wn = next_item(a, w + gridDim.x, W, nblk, nx);
+            TmaSrc<G> src;
+            src.base = base;
+            src.full = full;
+            src.empty = empty;
+            src.first = first;
+            src.status = status;
+            src.abort = abort;
+            src.k0 = it.k0;
+            src.p_last = it.p_last;
+            src.nsub = it.nsub;
+            src.a = &a;
+            src.nx = wn < W ? &nx : nullptr;
+            src.nq = qbuf + (qb ^ 1) * attn::kPairs * kHeadDim;
+            attn::UnitGeom ug;
+            ug.u = it.u;
+            ug.g = it.g;
+            ug.r0 = it.r0;
+            ug.P = it.nr * G;
+            ug.k0 = it.k0;
+            ug.nsub = it.nsub;
+            ug.p_first = it.p_first;
+            ug.p_last = it.p_last;
+            attn::unit_partial<G>(a, ug, smem_u32(qbuf + qb * attn::kPairs * kHeadDim), comb, src, bar);
+            if (wn >= W) break;
+            for (int i = 0; i < 4 * it.nsub; ++i) first.advance();
+            it = nx;
+            w = wn;
+            qb ^= 1;
+            cp_async_wait<0>();
+            bar();  // the next item's queries
+        }
+    }
+    __syncthreads();
+    if (*abort && tid == 0) __nanosleep(200000);  // copies already issued land before the CTA exits
+}
+
 // One CTA of 512 threads (a quarter of the units per 128) per (head, row).
 __global__ void __launch_bounds__(512) attn_merge_kernel(const __grid_constant__ AttnDecodeArgs a) {
     __shared__ float red[512 / 32];
@@ -200,6 +450,12 @@ cudaError_t init_attn_decode() {
                                          (int)sizeof(Smem));
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(attn_block_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+}
+
+cudaError_t init_attn_decode_tma() {
+    cudaError_t e = cudaFuncSetAttribute(attn_block_tma_kernel<7>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(attn_block_tma_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
 }
 
 int attn_decode_blocks(const AttnDecodeArgs& a, int* groups) {
@@ -230,6 +486,35 @@ cudaError_t launch_attn_block(const AttnDecodeArgs& a, cudaStream_t st, bool pdl
     c1.attrs = attr;
     c1.numAttrs = pdl ? 1 : 0;
     return G == 7 ? cudaLaunchKernelEx(&c1, attn_block_kernel<7>, a) : cudaLaunchKernelEx(&c1, attn_block_kernel<8>, a);
+}
+
+cudaError_t launch_attn_block_tma(const AttnDecodeArgs& a, const KvMaps& maps, int* status, cudaStream_t st,
+                                  bool pdl) {
+    const int G = a.n_q / a.n_kv;
+    if ((G != 7 && G != 8) || a.n_q % a.n_kv != 0) return cudaErrorInvalidValue;
+    int groups = 0;
+    const int nblk = attn_decode_blocks(a, &groups);
+    if (nblk > a.max_blocks) return cudaErrorInvalidValue;
+    static int sms = 0;  // one CTA per SM at most (the shared memory holds one)
+    if (sms == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const int W = nblk * a.n_kv * groups;  // work items
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t c = {};
+    c.gridDim = dim3(std::min(W, sms));
+    c.blockDim = dim3(kTThreads);
+    c.dynamicSmemBytes = kTSmem;
+    c.stream = st;
+    c.attrs = attr;
+    c.numAttrs = pdl ? 1 : 0;
+    return G == 7 ? cudaLaunchKernelEx(&c, attn_block_tma_kernel<7>, a, maps, nblk, W, status)
+                  : cudaLaunchKernelEx(&c, attn_block_tma_kernel<8>, a, maps, nblk, W, status);
 }
 
 cudaError_t launch_attn_merge(const AttnDecodeArgs& a, cudaStream_t st, bool pdl) {
