@@ -363,6 +363,17 @@ cudaError_t mv_launch(tfl_model* m, const MatvecArgs& e, const CUtensorMap* w0, 
     return launch_matvec_tma(a, m->grid, st, pdl);
 }
 
+// Decode attention partials: the TMA-fed kernel when every stream has one row
+// (one (row, head) tile per item: its consumers keep up with the ring), the
+// cp.async kernel otherwise (two-row items need the registers the producer
+// warp would take).  Both give the same bits.
+cudaError_t launch_attn_decode(const tfl_model* m, const AttnDecodeArgs& at, const KvMaps& maps, cudaStream_t st,
+                               bool pdl) {
+    bool one_row = true;
+    for (int s = 0; s < at.rows.n_streams; ++s) one_row = one_row && at.rows.row_start[s + 1] - at.rows.row_start[s] == 1;
+    return one_row ? launch_attn_block_tma(at, maps, m->status, st, pdl) : launch_attn_block(at, st, pdl);
+}
+
 // The layer stack over n rows described by rm (decode kernels).  Input: ids
 // (embedding gather) or h_in; output: the residual stream in m->h.
 int run_layers(tfl_model* m, const RowMap& rm, const KvMaps& maps, const int32_t* ids, const void* h_in,
@@ -416,7 +427,7 @@ int run_layers(tfl_model* m, const RowMap& rm, const KvMaps& maps, const int32_t
         at.n_kv = c.n_kv;
         at.layer = l;
         at.rows = rm;
-        LAUNCH(m, K_ATTN, st, launch_attn_block_tma(at, maps, m->status, st, pdl));
+        LAUNCH(m, K_ATTN, st, launch_attn_decode(m, at, maps, st, pdl));
         LAUNCH(m, K_MERGE, st, launch_attn_merge(at, st, pdl));
 
         MatvecArgs o = {};
@@ -1225,7 +1236,7 @@ int tfl_layer_op(tfl_model* m, int op, int layer, tfl_kv* kv, int pos0, int rows
             }
             KvMaps maps;
             maps.m[0] = kv->kvmap;
-            LAUNCH(m, K_ATTN, st, launch_attn_block_tma(at, maps, m->status, st, false));
+            LAUNCH(m, K_ATTN, st, launch_attn_decode(m, at, maps, st, false));
             LAUNCH(m, K_MERGE, st, launch_attn_merge(at, st, false));
             break;
         }
