@@ -45,11 +45,11 @@ def _run(m, logits, T, k, p, u):
     return ids.cpu().numpy(), st
 
 
-CONFIGS = [(0.6, 20, 0.95), (1.0, 0, 0.95), (0.6, 0, 1.0), (1.5, 50, 0.5), (0.3, 1, 1.0), (0.8, 3000, 0.9),
+SETTINGS = [(0.6, 20, 0.95), (1.0, 0, 0.95), (0.6, 0, 1.0), (1.5, 50, 0.5), (0.3, 1, 1.0), (0.8, 3000, 0.9),
            (2.0, 0, 0.3)]
 
 
-@pytest.mark.parametrize("T,k,p", CONFIGS)
+@pytest.mark.parametrize("T,k,p", SETTINGS)
 def test_sample_matches_oracle_tiny_vocab(orc, tiny_model, T, k, p):
     rows = 48
     logits = synth.normal_bf16(70, 1, (rows, TINY.vocab), 2.0, "cuda")
@@ -60,7 +60,7 @@ def test_sample_matches_oracle_tiny_vocab(orc, tiny_model, T, k, p):
     assert np.array_equal(got, ref), np.nonzero(got != ref)
 
 
-@pytest.mark.parametrize("T,k,p", CONFIGS[:4])
+@pytest.mark.parametrize("T,k,p", SETTINGS[:4])
 def test_sample_matches_oracle_33b_vocab(orc, big_model, T, k, p):
     rows = 16
     logits = synth.normal_bf16(72, 1, (rows, L1.vocab), 1.5, "cuda")
