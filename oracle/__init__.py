@@ -12,7 +12,9 @@ the C++ oracle; it does no arithmetic of its own.
 Parity status per function (what pins it; see tests/test_oracle_*.py):
   bf16 rounding ............ pinned (independent bit-twiddle + torch + brute force)
   rmsnorm .................. pinned (closed form, 2^k scaling, brute force)
-  linear ................... pinned (one-hot columns, exact small integers, brute force)
+  linear ................... pinned (one-hot columns, exact small integers, brute force);
+                             fp32-sum mode pinned against numpy's sequential fp32
+                             cumulative sum and a sum that fp32 visibly truncates
   rope table / apply ....... pinned (p = 0 identity, inv_freq[0] = 1, closed forms,
                              relative-position invariance, rotation really applied)
   attention ................ pinned (one key, equal keys, brute force, causality, MHA/MQA)
@@ -89,6 +91,27 @@ def set_threads(n: int) -> None:
 
 def get_threads() -> int:
     return int(lib().orc_get_threads())
+
+
+def set_fp32_sums(on: bool) -> None:
+    """Projection sums in fp32 (k increasing) instead of double; see orc_linear."""
+    lib().orc_set_fp32_sums(1 if on else 0)
+
+
+def get_fp32_sums() -> bool:
+    return bool(lib().orc_get_fp32_sums())
+
+
+class fp32_sums:
+    """Context manager: projection sums in fp32 inside the block."""
+
+    def __enter__(self):
+        self._old = get_fp32_sums()
+        set_fp32_sums(True)
+        return self
+
+    def __exit__(self, *exc):
+        set_fp32_sums(self._old)
 
 
 # ---- elementwise ------------------------------------------------------------

@@ -44,6 +44,12 @@
 namespace {
 
 int g_threads = 0;  // 0 = std::thread::hardware_concurrency()
+// Projection sums: 0 = in double (exact before the rounding point, the default
+// reading); 1 = in fp32, one IEEE addition per term in increasing k order (the
+// literal "fp32 sums rounded once" of the same pull request).  The second is a
+// second faithful implementation of the method whose distance from the first
+// measures how far two correct fp32-summing implementations may drift apart.
+int g_fp32_sums = 0;
 
 int thread_count() {
     if (g_threads > 0) return g_threads;
@@ -112,6 +118,8 @@ extern "C" {
 
 void orc_set_threads(int n) { g_threads = n; }
 int orc_get_threads(void) { return thread_count(); }
+void orc_set_fp32_sums(int on) { g_fp32_sums = on ? 1 : 0; }
+int orc_get_fp32_sums(void) { return g_fp32_sums; }
 
 // ---- elementwise primitives ------------------------------------------------
 
@@ -142,19 +150,28 @@ void orc_rmsnorm(const uint16_t* x, const uint16_t* w, int rows, int H, double e
 }
 
 // out[r][n] = bf16(sum_k W[n][k] * x[r][k]); W is [N][K] row-major (HF [out, in]).
-// Each sum runs over k in increasing order in double.
+// Each sum runs over k in increasing order, in double (default) or, with
+// orc_set_fp32_sums(1), in fp32 (a product of two bf16 numbers is exact in
+// fp32; each addition rounds to fp32).
 void orc_linear(const uint16_t* W, int N, int K, const uint16_t* x, int rows, uint16_t* out) {
     std::vector<double> xd((size_t)rows * K);
     for (size_t i = 0; i < xd.size(); ++i) xd[i] = bf16_val(x[i]);
+    const bool f32 = g_fp32_sums != 0;
     parallel_for(N, [&](long n) {
         const uint16_t* wn = W + n * (long)K;
         std::vector<double> wd(K);
         for (int k = 0; k < K; ++k) wd[k] = bf16_val(wn[k]);
         for (int r = 0; r < rows; ++r) {
             const double* xr = xd.data() + (size_t)r * K;
-            double acc = 0.0;
-            for (int k = 0; k < K; ++k) acc += wd[k] * xr[k];
-            out[(long)r * N + n] = bf16_round(acc);
+            if (f32) {
+                float acc = 0.0f;
+                for (int k = 0; k < K; ++k) acc = acc + (float)(wd[k] * xr[k]);
+                out[(long)r * N + n] = bf16_round((double)acc);
+            } else {
+                double acc = 0.0;
+                for (int k = 0; k < K; ++k) acc += wd[k] * xr[k];
+                out[(long)r * N + n] = bf16_round(acc);
+            }
         }
     });
 }

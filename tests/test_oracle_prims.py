@@ -185,6 +185,36 @@ def test_linear_small_integers_exact(orc):
     assert np.array_equal(got, want)
 
 
+def test_linear_fp32_sums_equal_sequential_fp32_cumsum(orc):
+    """fp32-sum mode: each output is numpy's sequential float32 cumulative sum of
+    the (exact) products in increasing k order, rounded to bf16 by torch."""
+    import torch
+    W = rand_bf16((12, 700), 1.0, 16)
+    x = rand_bf16((3, 700), 1.0, 17)
+    with orc.fp32_sums():
+        got = orc.linear(W, x)
+    assert not orc.get_fp32_sums()
+    Wv = _ref.bf16_to_float(W).astype(np.float32)
+    xv = _ref.bf16_to_float(x).astype(np.float32)
+    for r in range(3):
+        for n in range(12):
+            acc = np.cumsum(Wv[n] * xv[r], dtype=np.float32)[-1]
+            want = torch.tensor(acc, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).item() & 0xFFFF
+            assert got[r, n] == want, (r, n)
+
+
+def test_linear_fp32_sums_truncate_where_double_does_not(orc):
+    """1 + 2^20 x 2^-25: fp32 sums in increasing k order lose every small term
+    (1 + 2^-25 rounds back to 1), the double sum keeps them all (1 + 2^-5)."""
+    K = 1 + (1 << 20)
+    W = np.full((1, K), 0x3F80, np.uint16)                      # 1.0
+    x = np.full((1, K), _ref.f32_to_bf16_bits(np.float32(2.0 ** -25)), np.uint16)
+    x[0, 0] = 0x3F80
+    assert _ref.bf16_to_float(orc.linear(W, x))[0, 0] == 1.0 + 2.0 ** -5
+    with orc.fp32_sums():
+        assert _ref.bf16_to_float(orc.linear(W, x))[0, 0] == 1.0
+
+
 # ---- RoPE ---------------------------------------------------------------------
 
 THETA = 1.2e8
