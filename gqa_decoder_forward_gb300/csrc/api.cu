@@ -371,7 +371,7 @@ cudaError_t launch_attn_decode(const tfl_model* m, const AttnDecodeArgs& at, con
                                bool pdl) {
     bool one_row = true;
     for (int s = 0; s < at.rows.n_streams; ++s) one_row = one_row && at.rows.row_start[s + 1] - at.rows.row_start[s] == 1;
-    return one_row ? launch_attn_block_tma(at, maps, m->status, st, pdl) : launch_attn_block(at, st, pdl);
+    return one_row ? launch_attn_block_tma(at, maps, m->status, m->grid, st, pdl) : launch_attn_block(at, st, pdl);
 }
 
 // The layer stack over n rows described by rm (decode kernels).  Input: ids
@@ -1319,6 +1319,15 @@ int tfl_profile_read(tfl_model* m, int n_kinds, double* ms, long* launches) {
 }
 
 const char* tfl_profile_kind(int kind) { return (kind >= 0 && kind < K_COUNT) ? kKindName[kind] : nullptr; }
+
+int tfl_wait_probe(tfl_model* m, int which, int spin_limit, void* stream) {
+    if (!m) return fail(TFL_E_ARG, "NULL model");
+    if (which != 0 && which != 1) return fail(TFL_E_ARG, "which %d: 0 (grid barrier) or 1 (mbarrier)", which);
+    if (spin_limit < 1 || spin_limit > (1 << 20))
+        return fail(TFL_E_ARG, "spin_limit %d outside 1..%d", spin_limit, 1 << 20);
+    CK(launch_wait_probe(m->sync, m->status, which, (uint32_t)spin_limit, m->grid, (cudaStream_t)stream));
+    return ok();
+}
 
 int tfl_status(tfl_model* m, void* stream) {
     if (!m) return fail(TFL_E_ARG, "NULL model");

@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             TRing rp{0, 0u};
+            long long issued = 0;
             bool waited = false;
             for (int w = w0; w < W && !*abort; w = next_item(a, w + gridDim.x, W, nblk, it)) {
                 // an item whose keys all precede the stream's first row of this
@@ -376,10 +377,13 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
                         const int row0 = ((a.layer * 2 + (part >> 1)) * kv.n_pages + page) * kPage;
                         tma_load_3d(base + rp.stage * kTStage, &maps.m[it.s], (part & 1) * 64, it.g, row0,
                                     &full[rp.stage], pol);
+                        ++issued;
                         rp.advance();
                     }
                 }
             }
+            // after an abort, the copies already issued land before the CTA exits
+            if (*abort) drain_ring(full, kTDepth, rp.stage, rp.phase, issued, status);
         }
     } else {
         // ---- consumers: the eight warps of attn::unit_partial ----
@@ -431,7 +435,6 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
         }
     }
     __syncthreads();
-    if (*abort && tid == 0) __nanosleep(200000);  // copies already issued land before the CTA exits
 }
 
 // One CTA of 512 threads (a quarter of the units per 128) per (head, row).
@@ -488,20 +491,14 @@ cudaError_t launch_attn_block(const AttnDecodeArgs& a, cudaStream_t st, bool pdl
     return G == 7 ? cudaLaunchKernelEx(&c1, attn_block_kernel<7>, a) : cudaLaunchKernelEx(&c1, attn_block_kernel<8>, a);
 }
 
-cudaError_t launch_attn_block_tma(const AttnDecodeArgs& a, const KvMaps& maps, int* status, cudaStream_t st,
-                                  bool pdl) {
+cudaError_t launch_attn_block_tma(const AttnDecodeArgs& a, const KvMaps& maps, int* status, int sms,
+                                  cudaStream_t st, bool pdl) {
     const int G = a.n_q / a.n_kv;
-    if ((G != 7 && G != 8) || a.n_q % a.n_kv != 0) return cudaErrorInvalidValue;
+    if ((G != 7 && G != 8) || a.n_q % a.n_kv != 0 || sms < 1) return cudaErrorInvalidValue;
     int groups = 0;
     const int nblk = attn_decode_blocks(a, &groups);
     if (nblk > a.max_blocks) return cudaErrorInvalidValue;
-    static int sms = 0;  // one CTA per SM at most (the shared memory holds one)
-    if (sms == 0) {
-        int dev = 0;
-        cudaError_t e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
+    // one CTA per SM of the model's device at most (the shared memory holds one)
     const int W = nblk * a.n_kv * groups;  // work items
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

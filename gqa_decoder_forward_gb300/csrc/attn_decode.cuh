@@ -14,8 +14,10 @@ struct KvMaps {
 };
 
 cudaError_t init_attn_decode_tma();
-// status: the model's device status word (a bounded wait that gives up raises kStatusDevice).
-cudaError_t launch_attn_block_tma(const AttnDecodeArgs& a, const KvMaps& maps, int* status, cudaStream_t st,
-                                  bool pdl);
+// status: the model's device status word (a bounded wait that gives up raises
+// kStatusDevice); sms: the SM count of the model's device (the grid is at most
+// one CTA per SM).
+cudaError_t launch_attn_block_tma(const AttnDecodeArgs& a, const KvMaps& maps, int* status, int sms,
+                                  cudaStream_t st, bool pdl);
 
 }  // namespace tfl

@@ -64,6 +64,7 @@ constexpr int kSmem = 1024 + kOffBar + 16 * 8;
 
 struct Bars {
     uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], p_full[2], o_full[2];
+    uint64_t drain;  // MMA completion after an abort
     uint32_t tmem;
     int abort;
 };
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
             mbar_init(&b.p_full[i], 2 * kBM);
             mbar_init(&b.o_full[i], 1);
         }
+        mbar_init(&b.drain, 1);
         b.abort = 0;
         mbar_init_fence();
     }
@@ -131,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = b.tmem;
+    bool mma_any = false;  // the MMA thread issued at least one MMA
     pdl_wait();
 
     if (warp == kProducerWarp) {
@@ -143,12 +146,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
                 tma_load_2d(base + kOffQ + t * kTile, &a.qmap, h * kHeadDim, r0[t], &b.q_full, once);
                 tma_load_2d(base + kOffQ + t * kTile + kBox, &a.qmap, h * kHeadDim + 64, r0[t], &b.q_full, once);
             }
+            int issued = 0;  // key/value blocks whose copies were issued
             for (int j = 0; j < nb && !*abort; ++j) {
                 const int buf = j & 1;
                 if (j >= 2 && !mbar_wait(&b.kv_empty[buf], ((j >> 1) - 1) & 1, a.status)) {
                     *abort = 1;
                     break;
                 }
+                issued = j + 1;
                 const int page = __ldg(a.kv.table + j);
                 mbar_arrive_expect_tx(&b.kv_full[buf], 2 * kTile);
 #pragma unroll
@@ -158,6 +163,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
                     tma_load_3d(dst, &a.kvmap, 0, g, row0, &b.kv_full[buf], keep);
                     tma_load_3d(dst + kBox, &a.kvmap, 64, g, row0, &b.kv_full[buf], keep);
                 }
+            }
+            // after an abort, the copies already issued land before the CTA exits
+            // (blocks before the last two were released by the MMAs, so have landed)
+            if (*abort) {
+                mbar_wait(&b.q_full, 0u, a.status);
+                for (int j = issued >= 2 ? issued - 2 : 0; j < issued; ++j)
+                    mbar_wait(&b.kv_full[j & 1], (j >> 1) & 1, a.status);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -198,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
             // softmax.
             bool ok = mbar_wait(&b.q_full, 0, a.status) && kv_ready(0);
             if (ok) issue_s(0, 0);
+            mma_any = ok;
             for (int j = 0; j < nb && ok; ++j) {
                 if (j < nbt[0]) {
                     if (!(ok = mbar_wait(&b.p_full[0], j & 1, a.status))) break;
@@ -357,11 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
         }
     }
 
-    // every MMA was waited for by the softmax warps (or the kernel gave up): free TMEM
+    // every MMA was waited for by the softmax warps (or, after an abort, is waited
+    // for below): free TMEM
     tc_fence_before();
     __syncthreads();
     if (warp == kMmaWarp) {
-        if (*abort) __nanosleep(500000);  // let copies and MMAs already issued finish
+        // after an abort, every MMA already issued completes before tensor
+        // memory is freed (a commit tracks all of this thread's earlier MMAs)
+        if (lane == 0 && *abort && mma_any) {
+            tc_commit(&b.drain);
+            mbar_wait(&b.drain, 0u, a.status);
+        }
         tc_fence_after();
         __syncwarp();
         tmem_dealloc(tmem, kTmemCols);

@@ -192,6 +192,9 @@ __host__ __device__ inline int step_ts_stride(int layers) { return 2 + 2 * 6 * l
 int step_smem_bytes(int rows);
 cudaError_t init_step_persistent();
 cudaError_t launch_step_persistent(const StepArgs& a, int grid, cudaStream_t st);
+// The step kernel's bounded waits alone on events that never happen (which = 0:
+// grid barrier over `grid` CTAs; 1: mbarrier), giving up after `limit` polls.
+cudaError_t launch_wait_probe(unsigned* sync, int* status, int which, uint32_t limit, int grid, cudaStream_t st);
 
 // Seeded sampling (sample.cu); counts / wtab: per row 65,536 unsigned / double of scratch.
 cudaError_t launch_sample(const bf16* logits, int n_rows, int V, float temperature, int top_k, float top_p,

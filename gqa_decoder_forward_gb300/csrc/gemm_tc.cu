@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     uint64_t* acc_empty = acc_full + 2;       // [2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    uint64_t* drain = reinterpret_cast<uint64_t*>(tmem_slot + 2);  // MMA completion after an abort
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int total = a.m_tiles * a.n_tiles;
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 4);
         }
+        mbar_init(drain, 1);
         *s_abort = 0;
         mbar_init_fence();
     }
@@ -87,6 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    bool mma_any = false;  // the MMA thread issued at least one MMA
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -95,6 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             const uint64_t pa = policy_evict_last(), pb = policy_evict_first();
             int stage = 0;
             uint32_t phase = 0;
+            long long issued = 0;
             for (int t = blockIdx.x; t < total && !*s_abort; t += gridDim.x) {
                 const int n = t / a.m_tiles, m = t % a.m_tiles;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -119,12 +123,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     } else {
                         tma_load_2d(sB, &a.bmap[0], kb * 64, n * N, &full[stage], pb);
                     }
+                    ++issued;
                     if (++stage == C::kDepth) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
+            // after an abort, the copies already issued land before the CTA exits
+            if (*s_abort) drain_ring(full, C::kDepth, stage, phase, issued, a.status);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -134,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
             uint32_t phase = 0;
             int buf = 0;
             uint32_t acc_phase = 0;
+            bool any = false;
             for (int t = blockIdx.x; t < total && !*s_abort; t += gridDim.x) {
                 // the epilogue must have drained this accumulator
                 if (!mbar_wait(&acc_empty[buf], acc_phase ^ 1u, a.status)) {
@@ -154,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 #pragma unroll
                     for (int k = 0; k < 4; ++k)  // K = 16 per MMA: +32 bytes (2 in the >>4 address field)
                         tc_mma_bf16(d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+                    any = true;
                     tc_commit(&empty[stage]);
                     if (++stage == C::kDepth) {
                         stage = 0;
@@ -166,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     acc_phase ^= 1u;
                 }
             }
+            mma_any = any;
         }
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
@@ -280,11 +290,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         pdl_trigger();
     }
 
-    // all MMAs were waited for by the epilogue (or the kernel gave up): free TMEM
+    // all MMAs were waited for by the epilogue (or, after an abort, are waited
+    // for below): free TMEM
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
-        if (*s_abort) __nanosleep(500000);  // let copies and MMAs already issued finish
+        // after an abort, every MMA already issued completes before tensor
+        // memory is freed (a commit tracks all of this thread's earlier MMAs)
+        if (lane == 0 && *s_abort && mma_any) {
+            tc_commit(drain);
+            mbar_wait(drain, 0u, a.status);
+        }
         tc_fence_after();
         __syncwarp();
         tmem_dealloc(tmem, C::kTmemCols);

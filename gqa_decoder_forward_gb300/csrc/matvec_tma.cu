@@ -96,10 +96,12 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
             // kernels that produce the activations
             int pre_ks[8];
             int n_pre = 0;
+            long long issued = 0;
             while (n_pre < depth && t < tiles) {
                 mbar_arrive_expect_tx(&full[n_pre], stage_tx);
                 mvc::load_weights(a.e, a.wmap, t, ks * kKbPerStage, base + n_pre * stage_bytes, &full[n_pre], pw);
                 pre_ks[n_pre++] = ks;
+                ++issued;
                 if (++ks == nst) { ks = 0; t += gridDim.x; }
             }
             pdl_wait();
@@ -118,11 +120,12 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
                 mbar_arrive_expect_tx(&full[stage], stage_tx);
                 mvc::load_weights(a.e, a.wmap, t, ks * kKbPerStage, sA, &full[stage], pw);
                 if (!NORM) tma_load_3d(sA + kABytes, &a.xmap, 0, 0, ks * kKbPerStage, &full[stage], px);
+                ++issued;
                 if (++stage == depth) { stage = 0; phase ^= 1u; }
                 if (++ks == nst) { ks = 0; t += gridDim.x; }
             }
-            // after an abort, give copies already issued time to land before exiting
-            if (*s_abort) __nanosleep(500000);
+            // after an abort, the copies already issued land before the CTA exits
+            if (*s_abort) drain_ring(full, depth, stage, phase, issued, a.status);
         } else {
             pdl_wait();
             pdl_trigger();

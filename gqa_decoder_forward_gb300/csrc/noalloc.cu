@@ -86,8 +86,25 @@ extern "C" int tfl_attention_decode_noalloc(tfl_kv* kv, int layer, int pos0, int
         set_last_error(msg);
         return TFL_E_WORKSPACE;
     }
+    // the array used is the current device's copy: the cache must live there
+    int cur = -1;
+    cudaPointerAttributes pa = {};
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e == cudaSuccess) e = cudaPointerGetAttributes(&pa, view.pages);
+    if (e != cudaSuccess) {
+        snprintf(msg, sizeof msg, "tfl_attention_decode_noalloc: device query failed: %s", cudaGetErrorString(e));
+        set_last_error(msg);
+        return TFL_E_CUDA;
+    }
+    if (pa.type != cudaMemoryTypeDevice || pa.device != cur) {
+        snprintf(msg, sizeof msg,
+                 "tfl_attention_decode_noalloc: the cache is not device memory of the current device %d (it is on "
+                 "device %d); make the model's device current", cur, pa.device);
+        set_last_error(msg);
+        return TFL_E_ARG;
+    }
     float* scratch = nullptr;
-    cudaError_t e = scratch_for_current_device(&scratch);
+    e = scratch_for_current_device(&scratch);
     if (e != cudaSuccess) {
         snprintf(msg, sizeof msg, "tfl_attention_decode_noalloc: scratch set-up failed: %s", cudaGetErrorString(e));
         set_last_error(msg);

@@ -179,16 +179,22 @@ __device__ __forceinline__ int attn_groups(const StepArgs& a) {
     return g;
 }
 
-// Waits until the grid barrier counter reaches target; false on timeout or abort.
-__device__ __forceinline__ bool wait_counter(const StepArgs& a, unsigned target) {
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        if (ld_acquire(a.sync) >= target) return true;
-        if (*((volatile unsigned*)a.sync + 1) != 0u) return false;
+// Waits until the grid barrier counter sync[0] reaches target; false on
+// timeout or when another CTA has raised the abort flag sync[1].  A timeout
+// sets kStatusDevice and raises the abort flag, which ends every other wait.
+__device__ __forceinline__ bool wait_counter(unsigned* sync, int* status, unsigned target,
+                                             uint32_t limit = kSpinLimit) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        if (ld_acquire(sync) >= target) return true;
+        if (*((volatile unsigned*)sync + 1) != 0u) return false;
         if (i >= 32) __nanosleep(64);
     }
-    atomicOr(a.status, kStatusDevice);
-    atomicExch(a.sync + 1, 1u);
+    atomicOr(status, kStatusDevice);
+    atomicExch(sync + 1, 1u);
     return false;
+}
+__device__ __forceinline__ bool wait_counter(const StepArgs& a, unsigned target) {
+    return wait_counter(a.sync, a.status, target);
 }
 
 struct ConsumerBar {
@@ -209,18 +215,20 @@ struct RingPos {
 
 // ---- producer (warp 8, lane 0) ------------------------------------------------
 // Fills the ring in exactly the order the consumers drain it.
+// rp / issued: the next ring stage and the number of stages armed so far
+// (read by the caller to drain the ring after an abort).
 __device__ void producer(const StepArgs& a, unsigned char* ring, uint64_t* full, uint64_t* empty,
-                         volatile int* s_abort) {
+                         volatile int* s_abort, RingPos& rp, long long& issued) {
     const uint64_t pol = policy_evict_first();
     const int G = gridDim.x;
     const int nblk = attn_blocks(a), units = nblk * a.n_kv * attn_groups(a);
-    RingPos rp{0, 0u, ring_depth(a.rows.n_rows)};
     auto take = [&]() -> unsigned char* {
         if (*s_abort || !mbar_wait(&empty[rp.stage], rp.phase ^ 1u, a.status)) {
             *s_abort = 1;
             return nullptr;
         }
         mbar_arrive_expect_tx(&full[rp.stage], kStage);
+        ++issued;  // the copy into this stage follows at once
         return ring + rp.stage * kStage;
     };
     auto weights = [&](int l, int ph) -> bool {
@@ -498,16 +506,47 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     __syncthreads();
     if (warp == kConsumerWarps) {
         if (lane == 0) {
-            producer(a, ring, full, empty, s_abort);
-            // after an abort, give copies already issued time to land before the CTA ends
-            if (*s_abort) __nanosleep(500000);
+            RingPos rp{0, 0u, depth};
+            long long issued = 0;
+            producer(a, ring, full, empty, s_abort, rp, issued);
+            // after an abort, the copies already issued land before the CTA ends
+            if (*s_abort) drain_ring(full, rp.depth, rp.stage, rp.phase, issued, a.status);
         }
         return;
     }
     consumers(a, ring, xs, red, red_norm, full, empty, s_abort);
 }
 
+// The two bounded waits of the step kernel run alone, each on something that
+// never happens, so that their give-up path can be exercised: which = 0: the
+// grid-barrier wait of thread 0 of every CTA on a counter target no CTA
+// reaches (the first CTA to give up raises the abort flag, which ends the
+// others' waits); which = 1: an mbarrier wait on a phase that never receives
+// an arrival (no copy is issued to it).  Either way the status word gets
+// kStatusDevice and the kernel returns.
+__global__ void wait_probe_kernel(unsigned* sync, int* status, int which, uint32_t limit) {
+    __shared__ uint64_t bar;
+    if (which == 0) {
+        if (threadIdx.x == 0) wait_counter(sync, status, 0xFFFFFFFFu, limit);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0u, status, limit);
+    __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(unsigned* sync, int* status, int which, uint32_t limit, int grid, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
+    wait_probe_kernel<<<which == 0 ? grid : 1, 32, 0, st>>>(sync, status, which, limit);
+    return cudaGetLastError();
+}
 
 int step_smem_bytes(int rows) {
     return 1024 + ring_depth(rows) * kStage + xs_bytes(rows) + kRedBytes + 8 * kStepMaxRows * 4 + 2 * kMaxDepth * 8 + 64;

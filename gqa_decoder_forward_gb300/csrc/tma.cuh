@@ -46,15 +46,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
-// after about a second: sets kStatusDevice in *status and returns false, so a
-// broken pipeline ends the kernel instead of hanging the GPU.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
-    for (uint32_t i = 0; i < (1u << 24); ++i) {
+// after `limit` polls (by default about a second): sets kStatusDevice in
+// *status and returns false, so a broken pipeline ends the kernel instead of
+// hanging the GPU.
+constexpr uint32_t kMbarSpinLimit = 1u << 24;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          uint32_t limit = kMbarSpinLimit) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (i >= 16) __nanosleep(64);
     }
     atomicOr(status, kStatusDevice);
     return false;
+}
+
+// After an abort: waits, bounded, for the copies of the last `issued` (at
+// most depth) stages a producer armed on a ring of `depth` stages whose next
+// stage is (stage, phase), so that no copy lands in shared memory after the
+// CTA has exited.  Older stages were refilled only after their consumers
+// released them, so their copies have landed.  A wait that runs out leaves
+// kStatusDevice set.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int depth, int stage, uint32_t phase, long long issued,
+                                           int* status) {
+    const int n = issued < depth ? (int)issued : depth;
+    for (int i = 0; i < n; ++i) {
+        if (stage == 0) {
+            stage = depth - 1;
+            phase ^= 1u;
+        } else {
+            --stage;
+        }
+        mbar_wait(&full[stage], phase, status);
+    }
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -75,6 +75,7 @@ SIGNATURES = {
     "tfl_prefill_chunk": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp]),
     "tfl_argmax": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _vp, _vp]),
     "tfl_status": (ctypes.c_int, [_vp, _vp]),
+    "tfl_wait_probe": (ctypes.c_int, [_vp, ctypes.c_int, ctypes.c_int, _vp]),
     "tfl_decode_hidden": (ctypes.c_int, [_vp, ctypes.POINTER(_vp), ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                          _vp, _vp, _vp]),
     "tfl_prefill_hidden": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int, _vp, _vp]),
@@ -322,6 +323,12 @@ def tfl_argmax(model: Model, logits, ids, stream=None):
 
 def tfl_status(model: Model, stream=None) -> int:
     return int(lib().tfl_status(model.handle, _stream(stream)))
+
+
+def tfl_wait_probe(model: Model, which: int, spin_limit: int, stream=None):
+    """Runs one bounded device wait (0: grid barrier, 1: mbarrier) on an event
+    that never happens; tfl_status then reports TFL_E_DEVICE."""
+    return _check(lib().tfl_wait_probe(model.handle, int(which), int(spin_limit), _stream(stream)))
 
 
 TFL_OP_PROMPT = 0x100

@@ -120,7 +120,10 @@ size_t tfl_workspace_bytes(const tfl_config* cfg);
  * for max_context positions on the host and uploads it into the workspace
  * (synchronously, on the legacy default stream).  The workspace (16-byte
  * aligned device memory) is owned by the caller and used exclusively by this
- * model until tfl_free.
+ * model until tfl_free.  The refusal of other devices by name follows the
+ * pull request's refusal of GPUs without the tensor units its prompt path
+ * needs, checked at load before anything is mapped (pull request #1415,
+ * section "Checks", and the reply "No tensor units").
  */
 int tfl_init(const tfl_config* cfg, const tfl_weights* weights, void* workspace, size_t ws_bytes,
              tfl_model** out);
@@ -149,7 +152,10 @@ size_t tfl_kv_bytes(const tfl_config* cfg, int max_positions);
 /*
  * Creates a KV object over dev_buf (16-byte aligned, >= tfl_kv_bytes bytes,
  * owned by the caller).  1 <= max_positions <= cfg.max_context.  Writes the
- * identity page table (synchronously).  The length starts at 0.
+ * identity page table (synchronously).  The length starts at 0.  The cache is
+ * the position-major bf16 key/value cache of pull request #1415 ("How": prompt
+ * attention "over a position-major cache"; "bf16 keys and values"), sized by
+ * the caller as the served setup sizes it by --context.
  */
 int tfl_kv_alloc(tfl_model* model, int max_positions, void* dev_buf, size_t bytes, tfl_kv** out);
 void tfl_kv_free(tfl_kv* kv);
@@ -157,7 +163,8 @@ void tfl_kv_free(tfl_kv* kv);
 /*
  * Sets the length (number of valid positions) to keep, 0 <= keep <=
  * max_positions.  keep < length truncates to a kept prefix (resume: the next
- * call continues at position keep).  keep > length declares positions
+ * call continues at position keep; "a turn resumed from a kept prompt state
+ * equals the same request after a restart", pull request #1415, "Measured").  keep > length declares positions
  * [length, keep) valid; their contents must have been written by earlier calls
  * or by tfl_kv_write.  Host-only; enqueues nothing.
  */
@@ -211,7 +218,10 @@ int tfl_prefix_store_size(const tfl_prefix_store* store);
 /* ---- forward ------------------------------------------------------------------ */
 
 /*
- * One decode step over n_streams streams (1..16) sharing the weight pass.
+ * One decode step over n_streams streams (1..16) sharing the weight pass:
+ * the decode rows of pull request #1415, section "How" (row projections with
+ * fp32 sums rounded once, attention of each row over key blocks at absolute
+ * positions; the lane host's shared rounds of several streams).
  * Stream s contributes rows_per_stream[s] (host array, 1..16) consecutive rows
  * of ids (device int32 [sum rows], stream-major), at positions length(s) ..
  * length(s) + rows - 1; a multi-row group is a causal window (each row sees
@@ -239,7 +249,8 @@ int tfl_set_persistent(tfl_model* model, int enable);
 /*
  * Prompt chunk of n_rows (1..max_rows) ids (device int32) for one stream, at
  * positions length .. length + n_rows - 1 (causal over the cache and the
- * chunk).  logits: NULL for none; else device bf16 [1][V] for the last row
+ * chunk): the prompt chunks of up to 2,048 rows of pull request #1415, section
+ * "How" (projections as dense GEMMs, attention over the position-major cache).  logits: NULL for none; else device bf16 [1][V] for the last row
  * (all_rows == 0) or [n_rows][V] (all_rows != 0).  length += n_rows.
  * The row results do not depend on where chunk boundaries fall (a prompt
  * resumed from a kept prefix equals the same prompt prefilled fresh).
@@ -340,8 +351,28 @@ int tfl_copy_draft(const int32_t* tokens, int n, int max_draft, int32_t* out);
  * Synchronises `stream`, reads and clears the device status word: returns
  * TFL_OK, TFL_E_NONFINITE (an argmax saw a non-finite logit) or TFL_E_DEVICE
  * (a kernel gave up a bounded wait), or TFL_E_CUDA if the stream had failed.
+ * A non-finite row is refused rather than given an id, as the pages' judge
+ * refuses a row holding NaN or +-Inf before choosing a token (pull request
+ * #1415, the reply on non-finite rows of the teacher-forced checker).
  */
 int tfl_status(tfl_model* model, void* stream);
+
+/*
+ * Test aid for the failure path of the device waits: runs one of the bounded
+ * waits of the persistent decode step alone, on an event that never happens,
+ * with a poll limit of spin_limit (1..2^20; the kernels' own limit is 2^24,
+ * about a second):  which = 0: the grid-barrier wait (thread 0 of one CTA per
+ * SM on a counter target no CTA reaches; the first to give up raises the abort
+ * flag that ends the others' waits); which = 1: an mbarrier wait on a phase
+ * that receives no arrival (no copy is in flight).  The wait gives up, sets the
+ * device status word and the kernel returns, so the next tfl_status returns
+ * TFL_E_DEVICE and the model stays usable (the grid-barrier words are reset at
+ * every persistent step).  Enqueues on stream.  TFL_E_ARG for other values.
+ * No counterpart on the pages, whose refusals are host-side ("rejected the
+ * next token" past the cache, NInfer model card, "Validation"); this checks
+ * that a device-side give-up is likewise an error status and not a hang.
+ */
+int tfl_wait_probe(tfl_model* model, int which, int spin_limit, void* stream);
 
 /* ---- component entry points (the same kernels, for per-layer checks) ------- */
 

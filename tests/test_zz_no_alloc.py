@@ -62,3 +62,24 @@ def test_noalloc_attention_refuses_sizes_beyond_its_scratch():
     with pytest.raises(tfl.TflError) as e:
         tfl.tfl_attention_decode_noalloc(kv, 0, 20000, q, out)   # 16 rows x 56 heads x 40 units of 512 keys
     assert e.value.code == tfl.TFL_E_WORKSPACE and "16 MiB" in str(e.value)
+
+
+def test_noalloc_attention_near_its_limit():
+    """One 33B-shaped row at position 294,900: 56 heads x 576 units of 512 keys =
+    32,256 partials of the 32,263 the scratch holds; bit-equal to the workspace
+    attention on the same inputs."""
+    shape = synth.NANBEIGE_33B.with_layers(1)
+    pos0 = 294900
+    m = _attention_only_model(shape, pos0 + 64)
+    kv = m.kv(pos0 + 64)
+    K, V = synth.kv_contents(shape, 72, 0, pos0 + 1, "cuda")
+    kv.write(0, 0, K, V)
+    del K, V
+    qd = shape.n_q * shape.head_dim
+    q = synth.normal_bf16(73, 0, (1, qd), 1.7, "cuda")
+    ref = torch.empty((1, qd), dtype=torch.bfloat16, device="cuda")
+    tfl.tfl_layer_op(m, "attention", 0, q, ref, kv, pos0)
+    out = torch.full((1, qd), float("nan"), dtype=torch.bfloat16, device="cuda")
+    tfl.tfl_attention_decode_noalloc(kv, 0, pos0, q, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
