@@ -54,6 +54,8 @@ def parse():
                         "positions) instead of the default line")
     p.add_argument("--prompt", action="store_true",
                    help="--op runs the prompt-chunk kernel of the op (rows up to 2,048)")
+    p.add_argument("--concurrent-streams", type=int, default=16,
+                   help="streams of the concurrent figures of the default line (0 = skip them)")
     p.add_argument("--drafted-tokens", type=int, default=64,
                    help="greedy tokens for the drafted-decode figures of the default line (0 = skip them)")
     return p.parse_args()
@@ -211,20 +213,68 @@ def oracle_sample(context: int, min_seconds: float = 10.0):
 
 # ---- the two arms ---------------------------------------------------------------------
 
+def decode_config(args, world):
+    """The workload description both arms print (the driver compares them)."""
+    return {"workload": f"Nanbeige4.3-33B-shaped decode, {args.layers} layers, 1 stream x 1 row, "
+                        f"context {args.context} (+{args.warmup} warm-up)",
+            "context_mean": args.context + args.warmup + (args.steps - 1) / 2.0, "rows": 1, "streams": 1,
+            "layers": args.layers, "l2": "inputs larger than L2 (61.7 GiB of weights streamed per step)",
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def run_reference(args, world, rank):
+    """The oracle arm.  A timed step is a bounded sample of the decode step: one
+    33B-shaped decoder layer of the oracle (one row at the benchmark's context,
+    over a seeded cache), so the run ends in seconds.  --warmup untimed and
+    --steps timed samples; ms_per_step is the measured time of one sample, and
+    value extrapolates to the whole step: 1 / (layers x mean sample time + the
+    time of one lm_head row, measured once outside the timed samples)."""
     if rank != 0:
         return
+    import numpy as np
+
+    import oracle
+    oracle.build()
     ctx = args.context
-    per_tok, cores, desc, t_layer, t_head = oracle_sample(ctx, min_seconds=3.0)
-    # each timed step: one layer of the oracle (a bounded sample of the 52-layer step)
-    import numpy as np  # noqa: F401
-    value = 1.0 / per_tok
+    one = SHAPE.with_layers(1)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = {k: [synth.layer_weight(one, 21, 0, k, dev)] for k in synth.LAYER_KEYS}
+    hw = {k: [synth.bits(w[k][0])] for k in synth.LAYER_KEYS}
+    hw["embed"] = np.zeros(8, np.uint16)
+    hw["final_norm"] = synth.bits(synth.global_weight(one, 21, "final_norm", dev))
+    hw["lm_head"] = synth.bits(synth.global_weight(one, 21, "lm_head", dev))
+    del w
+    c = oracle.Config(one.hidden, 1, one.n_q, one.n_kv, one.head_dim, one.ffn, one.vocab, one.rope_theta,
+                      one.rms_eps)
+    om = oracle.Model(c, hw, ctx + 1)
+    K, V = synth.kv_contents(one, 12, 0, ctx, dev)
+    om.K[0, :ctx] = synth.bits(K)
+    om.V[0, :ctx] = synth.bits(V)
+    h = synth.bits(synth.hidden_rows(one, 13, 1, dev))
+    pos = np.array([ctx], np.int32)
+    for _ in range(args.warmup):
+        out = om.layer(0, h, pos)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        out = om.layer(0, h, pos)
+        times.append(time.perf_counter() - t0)
+    t1 = time.perf_counter()
+    om.head(out)
+    t_head = time.perf_counter() - t1
+    t_layer = sum(times) / len(times)
+    per_token = args.layers * t_layer + t_head
+    value = 1.0 / per_token
+    cores = oracle.get_threads()
+    desc = (f"oracle, {cores} threads: each timed step is one 33B-shaped decoder layer of the decode step (1 row at "
+            f"position {ctx}, seeded KV), {args.steps} timed after {args.warmup} untimed, mean "
+            f"{t_layer * 1e3:.1f} ms; value = 1 / ({args.layers} x that + one lm_head row {t_head * 1e3:.0f} ms)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_tok * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"Nanbeige4.3-33B-shaped decode, 1 stream, context {ctx}", "context": ctx,
-                   "rows": 1, "layers": SHAPE.layers},
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_layer * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (random-init weights, seeded KV)",
+        "config": decode_config(args, world),
+        "reference_step": f"one of {args.layers} layers per timed step; value extrapolated to the whole step",
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -431,6 +481,10 @@ def run_tfl(args, world, rank, local):
     if args.kv == "prefill" and args.drafted_tokens > 0:
         drafted = drafted_figures(model, kv, ids, first_id, ctx, args.drafted_tokens, dev)
 
+    conc = None
+    if args.concurrent_streams > 0 and args.kv == "prefill":
+        conc = default_concurrent(model, shape, args.concurrent_streams, ctx, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         per_tok, cores, desc, _, _ = oracle_sample(ctx, min_seconds=10.0)
@@ -441,11 +495,7 @@ def run_tfl(args, world, rank, local):
         "metric": METRIC, "value": round(value, 3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init weights, uniform-random ids)",
-        "config": {"workload": f"Nanbeige4.3-33B-shaped decode, {args.layers} layers, 1 stream x 1 row, "
-                               f"context {ctx} (+{args.warmup} warm-up)",
-                   "context_mean": mean_ctx, "rows": 1, "streams": 1, "layers": args.layers,
-                   "l2": "inputs larger than L2 (61.7 GiB of weights streamed per step)",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": decode_config(args, world),
         "step_hbm": {"bytes": step_b, "achieved_gbs": round(step_gbs, 1), "peak_gbs": peak,
                      "frac": round(step_gbs / peak, 4), "peak_kind": peak_kind},
         "roofline": roof,
@@ -465,10 +515,32 @@ def run_tfl(args, world, rank, local):
         "clocks": clk.summary(),
         "status": status,
         "drafted": drafted,
+        "concurrent": conc,
         "cpu_baseline": cpu,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def default_concurrent(model, shape, S, ctx, dev):
+    """The concurrent configuration of S streams at ctx tokens each: every stream
+    prefills its own uniform-random prompt (seed 41 + s) in 2,048-row chunks,
+    then decode steps of all S streams (one row each) are timed and checked
+    equal to each stream alone."""
+    cap = ctx + 3 + 16 + 1 + 4 + 4
+    kvs = [model.kv(cap) for _ in range(S)]
+    first = torch.empty(S, dtype=torch.int32, device=dev)
+    last = torch.empty((1, shape.vocab), dtype=torch.bfloat16, device=dev)
+    for s in range(S):
+        p = synth.uniform_ids(41 + s, ctx, shape.vocab, dev)
+        for c in range(0, ctx, 2048):
+            model.prefill_chunk(kvs[s], p[c:c + 2048].contiguous(), last if c + 2048 >= ctx else None)
+        model.argmax(last, first[s:s + 1])
+    res = concurrent_figures(model, kvs, first, 16, 3)
+    res["workload"] = f"{S} streams x 1 row, each after its own {ctx}-token uniform-random prompt (seeds 41..)"
+    del kvs
+    torch.cuda.empty_cache()
+    return res
 
 
 DRAFTER_LAYERS = 4
@@ -557,16 +629,90 @@ def drafted_figures(model, kv, ids, first_id, ctx, n, dev):
     return res
 
 
+def concurrent_figures(model, kvs, ids, steps, warmup, check_steps=4, clocks_index=None):
+    """Decode steps of S streams x 1 row (the concurrent configurations), timed
+    with CUDA events; then every stream's greedy ids (and logits) over
+    check_steps steps together are compared with the same stream run alone from
+    the same state ("each reply equal to its run alone")."""
+    from gqa_decoder_forward_gb300 import tfl
+    S = len(kvs)
+    V = model.shape.vocab
+    dev = ids.device
+    st = torch.cuda.current_stream()
+    logits = torch.empty((S, V), dtype=torch.bfloat16, device=dev)
+    cur = ids.clone()
+
+    def step():
+        model.decode_step(kvs, cur, [1] * S, logits)
+        model.argmax(logits, cur)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start = [kv.length for kv in kvs]
+    clk = ClockSampler(clocks_index) if clocks_index is not None else None
+    if clk:
+        clk.__enter__()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(st)
+    for _ in range(steps):
+        step()
+    t1.record(st)
+    torch.cuda.synchronize()
+    if clk:
+        clk.__exit__(None, None, None)
+    ms = t0.elapsed_time(t1) / steps
+    tfl.tfl_profile(model, True)
+    step()
+    prof = tfl.tfl_profile_read(model)
+    phases = tfl.tfl_step_phases(model) if S <= 2 else None
+    tfl.tfl_profile(model, False)
+    # equal to solo, from the state after the timed steps
+    base = [kv.length for kv in kvs]
+    first = cur.clone()
+    together = []
+    for _ in range(check_steps):
+        step()
+        together.append((logits.clone(), cur.clone()))
+    equal = True
+    for s in range(S):
+        kvs[s].reset(base[s])
+        c = first[s:s + 1].clone()
+        lg = torch.empty((1, V), dtype=torch.bfloat16, device=dev)
+        for t in range(check_steps):
+            model.decode_step([kvs[s]], c, [1], lg)
+            model.argmax(lg, c)
+            equal = equal and torch.equal(lg.view(torch.int16), together[t][0][s:s + 1].view(torch.int16)) \
+                and int(c.item()) == int(together[t][1][s].item())
+    shape = model.shape
+    mean_ctx = sum(start) / S + (steps - 1) / 2.0
+    w = step_bytes(shape, 0)
+    kvb = shape.layers * 2 * shape.n_kv * shape.head_dim * 2 * mean_ctx * S
+    peak, peak_kind = measured_peaks()
+    gbs = (w + kvb) / (ms / 1e3) / 1e9
+    out = {"streams": S, "context_start": start, "steps": steps, "warmup": warmup,
+           "path": "persistent" if S <= 2 else "launch per operation",
+           "tok_s": round(S * 1e3 / ms, 2), "ms_per_step": round(ms, 4), "bytes_per_step": int(w + kvb),
+           "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "peak_kind": peak_kind,
+           "equal_solo": bool(equal), "equal_solo_steps": check_steps, "status": model.status(),
+           "step_phases_us": phases,
+           "kernels_one_step": {k: {"ms": round(v[0], 4), "launches": v[1]} for k, v in prof.items() if v[1]}}
+    if clk:
+        out["clocks"] = clk.summary()
+    return out
+
+
 def run_concurrent(args):
     """Decode steps of S streams x 1 row over seeded caches of --context positions each
-    (the concurrent configurations: 2 x 131,072 and 16 x 8,192)."""
+    (the concurrent configurations: 2 x 131,072 and 16 x 8,192), with the
+    equal-to-solo check."""
     from gqa_decoder_forward_gb300 import build, tfl
     build.build()
     S, ctx = args.concurrent, args.context
     shape = SHAPE.with_layers(args.layers)
     dev = torch.device("cuda", torch.cuda.current_device())
     weights = synth.model_weights(shape, 21, dev)
-    extra = args.warmup + args.steps + 9
+    extra = args.warmup + args.steps + 16
     model = tfl.Model(shape, weights, max_rows=64, max_decode_rows=64, max_context=ctx + extra)
     kvs = [model.kv(ctx + extra) for _ in range(S)]
     for l in range(shape.layers):
@@ -577,43 +723,9 @@ def run_concurrent(args):
     for kv in kvs:
         kv.reset(ctx)
     ids = synth.uniform_ids(41, S, shape.vocab, dev)
-    logits = torch.empty((S, shape.vocab), dtype=torch.bfloat16, device=dev)
-    st = torch.cuda.current_stream()
-
-    def step():
-        model.decode_step(kvs, ids, [1] * S, logits)
-        model.argmax(logits, ids)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    with ClockSampler(0) as clk:
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(st)
-        for _ in range(args.steps):
-            step()
-        t1.record(st)
-        torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / args.steps
-    phases = None
-    tfl.tfl_profile(model, True)
-    step()
-    prof = tfl.tfl_profile_read(model)
-    if S <= 2:
-        phases = tfl.tfl_step_phases(model)
-    tfl.tfl_profile(model, False)
-    kernels = {k: {"ms": round(v[0], 4), "launches": v[1]} for k, v in prof.items() if v[1]}
-    mean_ctx = ctx + args.warmup + (args.steps - 1) / 2.0
-    w = step_bytes(shape, 0)
-    kvb = shape.layers * 2 * shape.n_kv * shape.head_dim * 2 * mean_ctx * S
-    peak, peak_kind = measured_peaks()
-    gbs = (w + kvb) / (ms / 1e3) / 1e9
-    print(json.dumps({"mode": "concurrent", "streams": S, "context": ctx, "layers": args.layers,
-                      "path": "persistent" if S <= 2 else "launch per operation",
-                      "tok_s": round(S * 1e3 / ms, 2), "ms_per_step": round(ms, 4), "bytes_per_step": int(w + kvb),
-                      "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4), "peak_kind": peak_kind,
-                      "status": model.status(), "step_phases_us": phases, "kernels_one_step": kernels,
-                      "clocks": clk.summary()}), flush=True)
+    res = concurrent_figures(model, kvs, ids, args.steps, args.warmup, clocks_index=0)
+    print(json.dumps({"mode": "concurrent", "context": ctx, "layers": args.layers, "kv": "seeded", **res}),
+          flush=True)
 
 
 def run_op(args):
