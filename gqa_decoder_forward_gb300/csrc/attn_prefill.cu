@@ -3,15 +3,16 @@
 // and the chunk's own earlier rows on the tensor units), one pass with an
 // online softmax, the products on the 5th-generation tensor cores.
 //
-// One CTA per (query head h, pair of 128-row tiles A and B), 576 threads:
-//   warps 0-7 softmax of tile A, warps 8-15 softmax of tile B: two threads per
-//            query row (tensor-memory lane = row of the tile), each over half
-//            the keys of a block and half the output dims, the row max and
-//            sum exchanged through shared memory;
-//   warp 16  TMA producer: both tiles' queries once, then the keys and values
+// One CTA per (query head h, pair of 128-row tiles A and B), 384 threads:
+//   warps 0-3 softmax of tile A, warps 4-7 softmax of tile B: one thread per
+//            query row (tensor-memory lane = row of the tile) holding the
+//            row's 128 scores of a block in registers;
+//   warp 8   TMA producer: both tiles' queries once, then the keys and values
 //            of KV head h / G block by block (a block = 128 positions = one
 //            cache page), double-buffered;
-//   warp 17  allocates tensor memory and issues the MMAs (one thread), per
+//   warps 10-11 idle (they complete the third warpgroup, whose registers the
+//            softmax warpgroups take over);
+//   warp 9   allocates tensor memory and issues the MMAs (one thread), per
 //            block and tile: S = Q K^T (M = 128 rows, N = 128 keys, fp32 in
 //            tensor memory), then O += P V (M = 128 rows, N = 128 dims) with the
 //            weights P read from tensor memory, where the softmax wrote them
@@ -44,7 +45,12 @@
 namespace tfl {
 namespace {
 
-constexpr int kThreads = 576;
+constexpr int kThreads = 384;
+// Registers: launched at 168 a thread (384 x 168 = 64,512); the producer/MMA
+// warpgroup (warps 8-11) drops to kRegsLow, the two softmax warpgroups rise to
+// kRegsHigh: 128 x 64 + 256 x 216 = 63,488 of the launch's 64,512.
+constexpr int kRegsLow = 64, kRegsHigh = 216;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * 168, "register split exceeds the launch's registers");
 constexpr int kBM = 128;                  // query rows per tile
 constexpr int kBN = kPage;                // keys per block: one cache page
 constexpr int kBox = 128 * 64 * 2;        // 16 KB: 128 rows x 64 columns, 128-byte swizzle
@@ -53,13 +59,11 @@ constexpr int kTmemCols = 512;            // S/P of A, S/P of B, O of A, O of B:
 constexpr float kScale = 0.12751743074640502f;  // log2(e) / sqrt(128)
 constexpr float kRescale = 8.f;           // lazy rescale threshold (log2 units)
 
-constexpr int kProducerWarp = 16, kMmaWarp = 17;
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
 
-// Shared memory (from a 1024-byte aligned base): Q[2], K[2], V[2], the row-max
-// exchange ([tile][block parity][half][row]) and row-sum exchange ([tile][half][row]), barriers.
+// Shared memory (from a 1024-byte aligned base): Q[2], K[2], V[2], barriers.
 constexpr int kOffQ = 0, kOffK = 2 * kTile, kOffV = 4 * kTile;
-constexpr int kOffX = 6 * kTile;
-constexpr int kOffBar = kOffX + (2 * 2 * 2 * 128 + 2 * 2 * 128) * 4;
+constexpr int kOffBar = 6 * kTile;
 constexpr int kSmem = 1024 + kOffBar + 16 * 8;
 
 struct Bars {
@@ -118,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
             mbar_init(&b.kv_full[i], 1);
             mbar_init(&b.kv_empty[i], 1);
             mbar_init(&b.s_full[i], 1);
-            mbar_init(&b.p_full[i], 2 * kBM);
+            mbar_init(&b.p_full[i], kBM);
             mbar_init(&b.o_full[i], 1);
         }
         mbar_init(&b.drain, 1);
@@ -136,7 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
     bool mma_any = false;  // the MMA thread issued at least one MMA
     pdl_wait();
 
-    if (warp == kProducerWarp) {
+    if (warp >= 8) {
+      // the third warpgroup: producer, MMA issuer, two idle warps
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+      if (warp == kProducerWarp) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const uint64_t keep = policy_evict_last(), once = policy_evict_first();
@@ -172,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
                     mbar_wait(&b.kv_full[j & 1], (j >> 1) & 1, a.status);
             }
         }
-    } else if (warp == kMmaWarp) {
+      } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16_f32(kBM, kBN);
@@ -233,97 +240,92 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
             }
             if (!ok) *abort = 1;
         }
+      }
     } else {
-        // ---------------- softmax: two threads per row ----------------
-        // warps 8t .. 8t+7 serve tile t; warp w covers tensor-memory lanes
-        // 32 (w mod 4) .. +31 (the rows) and half (w / 4) mod 2 of the columns
-        // (keys 64 hf .. 64 hf + 63 of S, dims 64 hf .. of O)
-        const int t = warp >> 3, hf = (warp >> 2) & 1;
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+        // ---------------- softmax: one thread per row ----------------
+        // warps 4t .. 4t+3 serve tile t; warp w covers tensor-memory lanes
+        // 32 (w mod 4) .. +31, i.e. rows of the tile, and holds a row's 128
+        // scores of a block in registers (one load round trip, no exchange
+        // with other threads)
+        const int t = warp >> 2;
         const int row = (warp & 3) * 32 + lane;
-        const int pos = min(p_first[t] + row, p_last[t]);  // rows past the chunk see only real keys
+        // this tile's geometry as scalars (a runtime index into the arrays would put them in local memory)
+        const int t_r0 = t ? r0[1] : r0[0], t_nr = t ? nr[1] : nr[0], t_nb = t ? nbt[1] : nbt[0];
+        const int pos = t ? min(p_first[1] + row, p_last[1]) : min(p_first[0] + row, p_last[0]);  // rows past the chunk see only real keys
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_off + t * 128, tO = tmem + lane_off + 256 + t * 128 + hf * 64;
-        float* xm = reinterpret_cast<float*>(base + kOffX) + t * (2 * 2 * kBM);  // [block parity][half][row]
+        const uint32_t tS = tmem + lane_off + t * 128, tO = tmem + lane_off + 256 + t * 128;
         float m = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < nbt[t]; ++j) {
+        for (int j = 0; j < t_nb; ++j) {
             if (ok && !*abort && !mbar_wait(&b.s_full[t], j & 1, a.status)) ok = false;
             tc_fence_after();
-            const int k0 = j * kBN, kh = k0 + hf * 64;  // first key of this thread's half
-            const bool whole = k0 + kBN - 1 <= pos;      // every key of the block is visible to the row
-            // pass 1: max of the visible raw scores of this half, then of the row
-            float mx = -INFINITY;
-            {
-                float v[64];
-                tmem_ld64(tS + hf * 64, v);
-                if (whole) {
+            const int k0 = j * kBN;
+            const bool whole = k0 + kBN - 1 <= pos;  // every key of the block is visible to the row
+            uint32_t sc[kBN];
+            tmem_ld64_async(tS, sc);
+            tmem_ld64_async(tS + 64, sc + 64);
+            tmem_ld_wait();
+            // keys past the row's position: score -inf, so that they take no part
+            // in the max and get weight 2^-inf = 0 (only the blocks on the diagonal)
+            if (!whole) {
 #pragma unroll
-                    for (int e = 0; e < 64; ++e) mx = fmaxf(mx, v[e]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 64; ++e)
-                        if (kh + e <= pos) mx = fmaxf(mx, v[e]);
-                }
+                for (int e = 0; e < kBN; ++e)
+                    if (k0 + e > pos) sc[e] = 0xFF800000u;
             }
-            float* xj = xm + (j & 1) * (2 * kBM);
-            xj[hf * kBM + row] = mx;
-            named_barrier(1 + t, 8 * 32);
-            mx = fmaxf(xj[row], xj[kBM + row]);
-            const float bmax = mx * kScale;
+            // block max (the scale is positive; a max is exact in any order)
+            float mq[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) mq[e] = __uint_as_float(sc[e]);
+#pragma unroll
+            for (int e = 8; e < kBN; ++e) mq[e & 7] = fmaxf(mq[e & 7], __uint_as_float(sc[e]));
+            const float bmax = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])),
+                                     fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7]))) * kScale;
             const bool rescale = bmax > m + kRescale;  // a new reference max (always on block 0)
             const float alpha = rescale ? ex2(m - bmax) : 1.f;
             // O holds blocks 0 .. j-1 (this block's S was issued after that P V
             // finished); tensor-memory loads and stores take the whole warp, so
             // rows that keep their reference rewrite O times 1
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    float v[32];
-                    tmem_ld32(tO + c * 32, v);
+#pragma unroll 1
+                for (int c = 0; c < kHeadDim / 16; ++c) {
+                    float v[16];
+                    tmem_ld16(tO + c * 16, v);
                     uint32_t w[16];
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(v[half * 16 + e] * alpha);
-                        tmem_st16(tO + c * 32 + half * 16, w);
-                    }
+                    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(v[e] * alpha);
+                    tmem_st16(tO + c * 16, w);
                 }
             }
             if (rescale) {
                 l *= alpha;
                 m = bmax;
             }
-            // pass 2: this half's weights (hi, lo) written over its scores; four
-            // running sums over keys 4i+0..3, added in order at the end
+            // weights p = 2^(s log2(e)/sqrt(128) - m), split into hi = bf16(p) and
+            // lo = bf16(p - hi) (both rounded to nearest, unbiased), written over
+            // the scores: for keys 32c .. 32c+31, hi in columns 32c .. 32c+15 and lo
+            // in 32c+16 .. 32c+31; four running sums over keys 4i+0..3, added in
+            // order at the end of the block
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int c = 2 * hf + h2;  // keys 32c .. 32c+31 of the block
-                float v[32];
-                tmem_ld32(tS + c * 32, v);
-                uint32_t hi[16], lo[16];
+            for (int c = 0; c < kBN / 32; ++c) {
+                uint32_t w[32];
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
-                    float p0 = ex2(fmaf(v[e], kScale, -m));
-                    float p1 = ex2(fmaf(v[e + 1], kScale, -m));
-                    if (!whole) {
-                        if (k0 + c * 32 + e > pos) p0 = 0.f;
-                        if (k0 + c * 32 + e + 1 > pos) p1 = 0.f;
-                    }
+                    const int k = 32 * c + e;
+                    const float p0 = ex2(fmaf(__uint_as_float(sc[k]), kScale, -m));
+                    const float p1 = ex2(fmaf(__uint_as_float(sc[k + 1]), kScale, -m));
                     ls[e & 3] += p0;
                     ls[(e + 1) & 3] += p1;
-                    // hi = bf16(p), lo = bf16(p - hi), both rounded to nearest (unbiased)
                     const __nv_bfloat162 hh = __floats2bfloat162_rn(p0, p1);
-                    hi[e / 2] = *reinterpret_cast<const uint32_t*>(&hh);
-                    lo[e / 2] = pack_rn(p0 - __low2float(hh), p1 - __high2float(hh));
+                    w[e / 2] = *reinterpret_cast<const uint32_t*>(&hh);
+                    w[16 + e / 2] = pack_rn(p0 - __low2float(hh), p1 - __high2float(hh));
                 }
-                // hi in columns 32c .. 32c+15, lo in 32c+16 .. 32c+31
-                tmem_st16(tS + c * 32, hi);
-                tmem_st16(tS + c * 32 + 16, lo);
+                tmem_st32(tS + c * 32, w);
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);  // this half's running sum
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // values past the CTA's last position: exact zeros (the cache there holds anything)
-            if (hf == 0 && j == nb - 1 && k0 + row > p_end) {
+            if (j == nb - 1 && k0 + row > p_end) {
                 const uint32_t vrow = su + kOffV + (j & 1) * kTile + row * 128;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
@@ -337,25 +339,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_prefill_kernel(const __grid_
             tc_fence_before();
             mbar_arrive(&b.p_full[t]);
         }
-        // the row's sum = first half's + second half's
-        float* xl = reinterpret_cast<float*>(base + kOffX) + 2 * (2 * 2 * kBM) + t * (2 * kBM);
-        xl[hf * kBM + row] = l;
-        named_barrier(1 + t, 8 * 32);
-        l = xl[row] + xl[kBM + row];
-        // the tile's last P V, then out = bf16(O / l) for this half's 64 dims
-        if (nbt[t] > 0) {
-            if (ok && !*abort && !mbar_wait(&b.o_full[t], (nbt[t] - 1) & 1, a.status)) ok = false;
+        // the tile's last P V, then out = bf16(O / l)
+        if (t_nb > 0) {
+            if (ok && !*abort && !mbar_wait(&b.o_full[t], (t_nb - 1) & 1, a.status)) ok = false;
             tc_fence_after();
         }
         pdl_trigger();
         if (!ok) *abort = 1;
-        if (nbt[t] > 0) {  // every lane loads (whole-warp instruction); rows of the chunk store
-            bf16* out = a.out + (size_t)(r0[t] + row) * a.n_q * kHeadDim + (size_t)h * kHeadDim + hf * 64;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
+        if (t_nb > 0) {  // every lane loads (whole-warp instruction); rows of the chunk store
+            bf16* out = a.out + (size_t)(t_r0 + row) * a.n_q * kHeadDim + (size_t)h * kHeadDim;
+#pragma unroll 1
+            for (int c = 0; c < kHeadDim / 32; ++c) {
                 float v[32];
                 tmem_ld32(tO + c * 32, v);
-                if (row < nr[t]) {
+                if (row < t_nr) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint4 w;

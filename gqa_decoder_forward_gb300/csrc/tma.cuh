@@ -45,16 +45,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase of `bar` with the given parity to complete.  Gives up
-// after `limit` polls (by default about a second): sets kStatusDevice in
-// *status and returns false, so a broken pipeline ends the kernel instead of
-// hanging the GPU.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase of `bar` with the given parity to complete.  Each
+// try_wait suspends the thread in hardware until the phase completes or a
+// short time limit passes, so the loop needs no sleep of its own and wakes as
+// soon as the phase completes.  Gives up after `limit` polls or about a second
+// (global timer), whichever comes first: sets kStatusDevice in *status and
+// returns false, so a broken pipeline ends the kernel instead of hanging the GPU.
 constexpr uint32_t kMbarSpinLimit = 1u << 24;
+constexpr uint64_t kMbarWaitNs = 1000000000ull;
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           uint32_t limit = kMbarSpinLimit) {
-    for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (i >= 16) __nanosleep(64);
+        if ((i & 255u) == 0u && global_ns() - t0 > kMbarWaitNs) break;
     }
     atomicOr(status, kStatusDevice);
     return false;
