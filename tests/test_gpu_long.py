@@ -52,10 +52,11 @@ def long33():
 def _attn_bound(orc, qb, pos, Kb, Vb, ref):
     """1 ulp of the output plus, times sum_t p_t |v_t|, the fp32 accumulation
     allowance sqrt(keys) 2^-24 and the representation error of the weights as
-    bf16 hi + lo (2^-18 relative)."""
+    bf16 hi + lo (2^-16 relative: |p - hi| <= 2^-8 p, and lo = bf16(p - hi) is
+    within 2^-8 of p - hi, two roundings to 8 significant bits)."""
     absum = gu.bf16_to_f64(orc.attention(qb, pos, Kb, gu.abs_bits(Vb)))
     keys = (pos.astype(np.float64) + 1.0)[:, None]
-    return gu.ulp_of(ref) + (np.sqrt(keys) * 2.0 ** -24 + 2.0 ** -18) * absum
+    return gu.ulp_of(ref) + (np.sqrt(keys) * 2.0 ** -24 + 2.0 ** -16) * absum
 
 
 def _check_attention(orc, got, qb, pos, Kb, Vb, what):
