@@ -180,14 +180,21 @@ __device__ __forceinline__ int attn_groups(const StepArgs& a) {
 }
 
 // Waits until the grid barrier counter sync[0] reaches target; false on
-// timeout or when another CTA has raised the abort flag sync[1].  A timeout
-// sets kStatusDevice and raises the abort flag, which ends every other wait.
+// timeout or when another CTA has raised the abort flag sync[1].  One thread
+// per CTA polls (acquire loads, no sleep: the wake-up follows the last arrival
+// by one load); it gives up after `limit` polls or about a second of global
+// time, whichever comes first.  A timeout sets kStatusDevice and raises the
+// abort flag, which ends every other wait.
 __device__ __forceinline__ bool wait_counter(unsigned* sync, int* status, unsigned target,
                                              uint32_t limit = kSpinLimit) {
-    for (uint32_t i = 0; i < limit; ++i) {
+    if (ld_acquire(sync) >= target) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < limit; ++i) {
         if (ld_acquire(sync) >= target) return true;
-        if (*((volatile unsigned*)sync + 1) != 0u) return false;
-        if (i >= 32) __nanosleep(64);
+        if ((i & 63u) == 0u) {
+            if (*((volatile unsigned*)sync + 1) != 0u) return false;
+            if (global_ns() - t0 > kMbarWaitNs) break;
+        }
     }
     atomicOr(status, kStatusDevice);
     atomicExch(sync + 1, 1u);
