@@ -154,6 +154,51 @@ __device__ __forceinline__ void accumulate_stages(const MatvecArgs& e, float (&a
     }
 }
 
+// The same for a stage that holds two tiles' weights (tile A at sA, tile B at
+// sA + kABytes) and one activation box after them (at sA + 2 kABytes): each
+// warp reads its activation fragments once and runs the same mma sequence on
+// both tiles, so every output element accumulates exactly as in
+// accumulate_stages.  XFromStage-style fragments only (sX is passed).
+template <int NT, class XFrag>
+__device__ __forceinline__ void accumulate_stages_pair(const MatvecArgs& e, float (&acc)[2][NT][4], int ks0, int ks1,
+                                                       uint32_t base_u, int stage_bytes, int depth, int& stage,
+                                                       uint32_t& phase, uint64_t* full, uint64_t* empty,
+                                                       volatile int* s_abort, int* status, XFrag xfrag) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, tig = lane & 3;
+    const bool two_boxes = e.mode == MV_SWIGLU || e.mode == MV_QKV_ROPE;
+    const int line_lo = two_boxes ? warp * 8 + g : warp * 16 + g;
+    const int line_hi = two_boxes ? (kABytes / 2) / 128 + warp * 8 + g : warp * 16 + 8 + g;
+    for (int ks = ks0; ks < ks1; ++ks) {
+        if (!*s_abort && !mbar_wait(&full[stage], phase, status)) *s_abort = 1;
+        const uint32_t sA = base_u + stage * stage_bytes;
+        const uint32_t sX = sA + 2 * kABytes;
+        const int kb = ks * kKbPerStage + warp;  // this warp's k-block
+        uint4 l0[2], l1[2], h0[2], h1[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            line_chunks(sA + t * kABytes, line_lo, tig, l0[t], l1[t]);
+            line_chunks(sA + t * kABytes, line_hi, tig, h0[t], h1[t]);
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int xr = n * 8 + g;  // activation row of this lane's B fragment
+            uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
+            xfrag(xr, kb, sX, x0, x1);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                mma16816(acc[t][n], l0[t].x, h0[t].x, l0[t].y, h0[t].y, x0.x, x0.y);
+                mma16816(acc[t][n], l0[t].z, h0[t].z, l0[t].w, h0[t].w, x0.z, x0.w);
+                mma16816(acc[t][n], l1[t].x, h1[t].x, l1[t].y, h1[t].y, x1.x, x1.y);
+                mma16816(acc[t][n], l1[t].z, h1[t].z, l1[t].w, h1[t].w, x1.z, x1.w);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (++stage == depth) { stage = 0; phase ^= 1u; }
+    }
+}
+
 // Sums the eight warps' accumulators of tile t in warp order and runs the
 // epilogue for the R activation rows.  bar() synchronises the 256 consumer threads.
 template <int NT, class Bar>

@@ -160,6 +160,126 @@ __global__ void __launch_bounds__(kThreads, 1) matvec_tma_kernel(const __grid_co
     }
 }
 
+// Paired stages for 9 to 32 activation rows: a stage holds the weights of two
+// adjacent tiles (2u and 2u+1) and one activation box, so each activation box
+// streamed into shared memory serves 32 weight rows instead of 16 (at 16 rows
+// the unpaired stage moves as many activation bytes as weight bytes).  Each
+// tile's accumulation and cross-warp sum are those of matvec_tma_kernel, so
+// the results are bit-identical to it.  Requires an even tile count.
+__host__ __device__ constexpr int pair_stage_bytes(int x_rows_box) { return 2 * kABytes + x_rows_box * 1024; }
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1) matvec_tma_pair_kernel(const __grid_constant__ MatvecTmaArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* base =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int depth = a.depth;
+    const int stage_bytes = pair_stage_bytes(a.x_rows_box);
+    float* red = reinterpret_cast<float*>(base + depth * stage_bytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(red + kConsumerWarps * NT * 4 * 32);
+    uint64_t* empty = full + depth;
+    volatile int* s_abort = reinterpret_cast<volatile int*>(empty + depth);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units = a.tiles / 2, nst = a.kstages;
+    const uint32_t stage_tx = 2 * kABytes + a.x_rows_box * 128 * kKbPerStage;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < depth; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        *s_abort = 0;
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            const uint64_t pw = policy_evict_first(), px = policy_evict_last();
+            int u = blockIdx.x, ks = 0;
+            auto weights = [&](unsigned char* sA, uint64_t* bar) {
+                mvc::load_weights(a.e, a.wmap, 2 * u, ks * kKbPerStage, sA, bar, pw);
+                mvc::load_weights(a.e, a.wmap, 2 * u + 1, ks * kKbPerStage, sA + kABytes, bar, pw);
+            };
+            // weight stages that fit the ring are issued before waiting for the
+            // kernels that produce the activations
+            int pre_ks[8];
+            int n_pre = 0;
+            long long issued = 0;
+            while (n_pre < depth && u < units) {
+                mbar_arrive_expect_tx(&full[n_pre], stage_tx);
+                weights(base + n_pre * stage_bytes, &full[n_pre]);
+                pre_ks[n_pre++] = ks;
+                ++issued;
+                if (++ks == nst) { ks = 0; u += gridDim.x; }
+            }
+            pdl_wait();
+            pdl_trigger();
+            for (int i = 0; i < n_pre; ++i)
+                tma_load_3d(base + i * stage_bytes + 2 * kABytes, &a.xmap, 0, 0, pre_ks[i] * kKbPerStage, &full[i],
+                            px);
+            int stage = n_pre % depth;
+            uint32_t phase = n_pre == depth ? 1u : 0u;
+            while (u < units) {
+                if (*s_abort || !mbar_wait(&empty[stage], phase ^ 1u, a.status)) {
+                    *s_abort = 1;
+                    break;
+                }
+                unsigned char* sA = base + stage * stage_bytes;
+                mbar_arrive_expect_tx(&full[stage], stage_tx);
+                weights(sA, &full[stage]);
+                tma_load_3d(sA + 2 * kABytes, &a.xmap, 0, 0, ks * kKbPerStage, &full[stage], px);
+                ++issued;
+                if (++stage == depth) { stage = 0; phase ^= 1u; }
+                if (++ks == nst) { ks = 0; u += gridDim.x; }
+            }
+            // after an abort, the copies already issued land before the CTA exits
+            if (*s_abort) drain_ring(full, depth, stage, phase, issued, a.status);
+        } else {
+            pdl_wait();
+            pdl_trigger();
+        }
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    pdl_wait();
+    pdl_trigger();
+    const int tig = lane & 3;
+    const int R = a.e.n_rows, xrows = a.x_rows_box;
+    const uint32_t base_u = smem_u32(base);
+    const mvc::NamedBar1 bar;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        float acc[2][NT][4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int n = 0; n < NT; ++n) acc[t][n][0] = acc[t][n][1] = acc[t][n][2] = acc[t][n][3] = 0.f;
+        mvc::accumulate_stages_pair<NT>(a.e, acc, 0, nst, base_u, stage_bytes, depth, stage, phase, full, empty,
+                                        s_abort, a.status, mvc::XFromStage{xrows, warp, tig});
+        mvc::finish_tile<NT>(a.e, a.e.rows, 2 * u, R, acc[0], red, bar);
+        mvc::finish_tile<NT>(a.e, a.e.rows, 2 * u + 1, R, acc[1], red, bar);
+    }
+}
+
+template <int NT>
+cudaError_t launch_pair(const MatvecTmaArgs& a, int grid, cudaStream_t st, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes(NT, false, a.depth, pair_stage_bytes(a.x_rows_box), 0);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, matvec_tma_pair_kernel<NT>, a);
+}
+
 template <int NT, bool NORM>
 cudaError_t launch_nt(const MatvecTmaArgs& a, int grid, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
@@ -199,6 +319,10 @@ cudaError_t init_matvec_tma() {
         return e;
     if ((e = cudaFuncSetAttribute(matvec_tma_kernel<8, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)))
         return e;
+    if ((e = cudaFuncSetAttribute(matvec_tma_pair_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)))
+        return e;
+    if ((e = cudaFuncSetAttribute(matvec_tma_pair_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx)))
+        return e;
     return cudaFuncSetAttribute(matvec_tma_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
 }
 
@@ -225,8 +349,16 @@ cudaError_t launch_matvec_tma(const MatvecTmaArgs& a0, int grid, cudaStream_t st
         a.x_rows_box != matvec_tma_x_rows(a.e.n_rows) || a.e.K % 64 != 0 ||
         a.kstages != (a.e.K + 64 * kKbPerStage - 1) / (64 * kKbPerStage))
         return cudaErrorInvalidValue;
-    if (grid > a.tiles) grid = a.tiles;
     const bool norm = a.norm_w != nullptr;
+    if (!norm && (nt == 2 || nt == 4) && a.tiles % 2 == 0) {
+        // paired stages: each activation box serves two tiles
+        const int sb = pair_stage_bytes(a.x_rows_box);
+        a.depth = ring_depth(sb, kRing);
+        if (smem_bytes(nt, false, a.depth, sb, 0) > 227 * 1024) return cudaErrorInvalidValue;
+        if (grid > a.tiles / 2) grid = a.tiles / 2;
+        return nt == 2 ? launch_pair<2>(a, grid, st, pdl) : launch_pair<4>(a, grid, st, pdl);
+    }
+    if (grid > a.tiles) grid = a.tiles;
     a.depth = matvec_depth(a.e.n_rows, a.e.K, norm);
     const int sb = stage_bytes_of(a.x_rows_box, norm);
     if (smem_bytes(nt, norm, a.depth, sb, norm ? a.e.n_rows * a.e.K * 2 : 0) > 227 * 1024)
