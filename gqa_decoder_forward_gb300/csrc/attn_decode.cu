@@ -197,11 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_block_kernel(const __grid_co
 
 constexpr int kTConsumerWarps = 8;
 constexpr int kTThreads = (kTConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kTDepth = 8;                             // ring stages
+// One-row streams only: an item has at most 8 (row, head) pairs, so the combine
+// scratch is that of 8 pairs and the shared memory it frees goes to the ring.
+constexpr int kTDepth = 11;                            // ring stages
+constexpr int kTCombFloats = attn::comb_floats(8);
 constexpr int kTStage = kSub * 64 * 2;                 // 16 KB: 128 positions x 64 dims
 constexpr int kTOffQ = kTDepth * kTStage;              // two query buffers (4 KB each)
 constexpr int kTOffComb = kTOffQ + 2 * attn::kPairs * kHeadDim * 2;
-constexpr int kTOffBar = kTOffComb + attn::kCombFloats * 4;
+constexpr int kTOffBar = kTOffComb + kTCombFloats * 4;
 constexpr int kTSmem = 1024 + kTOffBar + (2 * kTDepth + 2) * 8;
 static_assert(kSub == kPage, "a sub-block is one cache page");
 static_assert(kTSmem <= 227 * 1024, "shared memory");
@@ -495,6 +498,8 @@ cudaError_t launch_attn_block_tma(const AttnDecodeArgs& a, const KvMaps& maps, i
                                   cudaStream_t st, bool pdl) {
     const int G = a.n_q / a.n_kv;
     if ((G != 7 && G != 8) || a.n_q % a.n_kv != 0 || sms < 1) return cudaErrorInvalidValue;
+    for (int s = 0; s < a.rows.n_streams; ++s)  // the combine scratch holds one row's pairs
+        if (a.rows.row_start[s + 1] - a.rows.row_start[s] != 1) return cudaErrorInvalidValue;
     int groups = 0;
     const int nblk = attn_decode_blocks(a, &groups);
     if (nblk > a.max_blocks) return cudaErrorInvalidValue;
