@@ -285,6 +285,33 @@ def test_33b_layer_steps_equal_windows(layer33, R):
     assert torch.equal(va.view(torch.int16), vb.view(torch.int16))
 
 
+@pytest.mark.parametrize("rows", [[16, 8], [16, 16], [16, 16, 16]], ids=["24", "32", "48"])
+def test_33b_layer_wide_steps_equal_one_row_steps_and_match_oracle(orc, layer33, rows):
+    """Steps of 17-64 rows in all (several streams of up to 16 rows, each a causal
+    window) run the projections with 32- and 64-row activation boxes (paired
+    weight stages up to 32 rows): every stream's rows equal the same rows run as
+    one-row steps bit for bit, and every op matches the oracle at that many rows."""
+    w, hw, K, V = layer33
+    R = sum(rows)
+    m = tfl.Model(L1, w, max_decode_rows=64, max_rows=64, max_context=4224)
+    h_in = synth.hidden_rows(L1, 17, R, "cuda")
+    kvs = [_seeded(m, K, V, 4224) for _ in rows]
+    wide = torch.empty_like(h_in)
+    tfl.tfl_decode_hidden(m, kvs, rows, h_in, wide)
+    r0 = 0
+    for n in rows:
+        kv = _seeded(m, K, V, 4224)
+        for i in range(n):
+            one = torch.empty_like(h_in[:1])
+            tfl.tfl_decode_hidden(m, [kv], [1], h_in[r0 + i:r0 + i + 1].contiguous(), one)
+            assert torch.equal(one.view(torch.int16), wide[r0 + i:r0 + i + 1].view(torch.int16)), (r0, i)
+        r0 += n
+    kv = _seeded(m, K, V, 4224)
+    pos = np.arange(4096, 4096 + R, dtype=np.int32)
+    ch = gu.oracle_chain(orc, L1, hw, 0, synth.bits(h_in), pos, synth.bits(K), synth.bits(V))
+    gu.check_ops(tfl, m, kv, 0, ch, 4096)
+
+
 # ---- the prompt-chunk path (tensor-core GEMM projections) -------------------------------
 
 @pytest.mark.parametrize("R", [1, 200])
