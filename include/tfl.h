@@ -351,7 +351,7 @@ int tfl_copy_draft(const int32_t* tokens, int n, int max_draft, int32_t* out);
  * Synchronises `stream`, reads and clears the device status word: returns
  * TFL_OK, TFL_E_NONFINITE (an argmax saw a non-finite logit) or TFL_E_DEVICE
  * (a kernel gave up a bounded wait), or TFL_E_CUDA if the stream had failed.
- * A non-finite row is refused rather than given an id, as the pages' judge
+ * A non-finite row is refused rather than given an id, as the pages' checker
  * refuses a row holding NaN or +-Inf before choosing a token (pull request
  * #1415, the reply on non-finite rows of the teacher-forced checker).
  */

@@ -47,7 +47,7 @@ TF_POSITIONS = 64
 
 def _fidelity(ref, got):
     """KL(ref || got) mean over positions, max |delta logit|, and top-1 agreement
-    under the pages' near-tie judge (a differing winner counts as agreeing when
+    under the pages' near-tie rule (a differing winner counts as agreeing when
     both sides' two contenders are within one bf16 step)."""
     fr, fg = gu.bf16_to_f64(ref), gu.bf16_to_f64(got)
     tr, tg = fr.argmax(-1), fg.argmax(-1)
