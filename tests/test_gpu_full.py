@@ -70,12 +70,16 @@ def test_full_model_teacher_forced_depth_sweep(orc, full):
     stay within 1.5x of that floor's KL and max |delta logit| at every depth and
     lose at most two more top-1 positions (near-tie rule) than it; where the
     floor is at the pages' own figures (depths 1 and 2) the GPU must reach top-1
-    >= 99% and, at depth 1, mean KL <= 1e-4."""
+    >= 99% and, at depth 1, mean KL <= 1e-4.  The residual stream after the
+    last layer of each depth is judged the same way: relative rms difference
+    within 1.5x of the floor's, and the share of elements within 1 bf16 ulp at
+    least 0.8x the floor's."""
     w, _, kvK, kvV = full
     V = FULL.vocab
     cap = CTX + TF_POSITIONS + 8
     ids = synth.uniform_ids(26, TF_POSITIONS, V, "cuda")
-    gpu = {}
+    gpu, gpu_h = {}, {}
+    emb = w["embed"][ids.long()].contiguous()        # the rows' embeddings (the residual stream's start)
     for d in DEPTHS:
         wd = {k: w[k] for k in ("embed", "final_norm", "lm_head")}
         for k in synth.LAYER_KEYS:
@@ -90,7 +94,15 @@ def test_full_model_teacher_forced_depth_sweep(orc, full):
             m.decode_step([kv], ids[t:t + 1].contiguous(), [1], lg[t:t + 1])
         assert m.status() == tfl.TFL_OK
         gpu[d] = synth.bits(lg)
-        del m, kv, lg
+        kv = m.kv(cap)
+        for l in range(d):
+            kv.write(l, 0, kvK[l], kvV[l])
+        kv.reset(CTX)
+        hid = torch.empty_like(emb)
+        for t in range(TF_POSITIONS):
+            tfl.tfl_decode_hidden(m, [kv], [1], emb[t:t + 1], hid[t:t + 1])
+        gpu_h[d] = synth.bits(hid)
+        del m, kv, lg, hid
     hw = gu.host_weights(w)
     om = gu.oracle_model(orc, FULL, hw, cap)
     for l in range(FULL.layers):
@@ -114,6 +126,13 @@ def test_full_model_teacher_forced_depth_sweep(orc, full):
             assert g["top1"] >= 0.99, (d, g)
         if d == 1:
             assert g["kl"] <= 1e-4, g
+        # the residual stream after d layers
+        gr, fr = gu.rel_rms(gpu_h[d], tr[d]), gu.rel_rms(tr32[d], tr[d])
+        gq = float(np.mean(gu.ulp_dist(gpu_h[d], tr[d]) <= 1))
+        fq = float(np.mean(gu.ulp_dist(tr32[d], tr[d]) <= 1))
+        print(f"          hidden: GPU rel rms {gr:.4f}, within 1 ulp {gq:.3f} | fp32-sum oracle {fr:.4f}, {fq:.3f}")
+        assert gr <= 1.5 * fr, (d, gr, fr)
+        assert gq >= 0.8 * fq, (d, gq, fq)
 
 
 @pytest.mark.parametrize("layer", [0, 25, 51])
