@@ -2,7 +2,7 @@
 // the persistent decode-step kernel so that both give the same bits.
 //
 // Unit partial (512 keys at absolute positions, one KV head, a group of up to
-// two rows): warp w of eight owns keys 16w..16w+15 of each 128-key sub-block
+// two rows, or four in the kernel that serves streams of several rows): warp w of eight owns keys 16w..16w+15 of each 128-key sub-block
 // and runs an online softmax over them (S = Q K^T scaled by log2(e)/sqrt(128)
 // and causally masked, running max, weights p = 2^(s - max) split into hi/lo
 // bf16, running sums, O = P V); the warp partials are then combined in warp
@@ -21,6 +21,18 @@ namespace attn {
 constexpr int kWarps = 8;            // warps taking part (256 threads)
 constexpr int kKB = kPage;           // keys per block
 constexpr float kScale = 0.12751743074640502f;  // log2(e) / sqrt(128)
+// A warp's reference max for a pair moves only when a sub-block's max exceeds
+// it by more than kLazy (log2 units), so its weights stay <= 2^kLazy and the
+// running output is rescaled only then.
+constexpr float kLazy = 8.f;
+
+// 2^x by the special-function unit (approximate, flushes subnormal results to
+// zero; 2^-inf = 0).
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Rows of 128 bf16 (256 bytes, 16 chunks of 16 bytes) with chunk c of row r
 // stored at chunk c ^ (r & 7): the eight rows an ldmatrix reads hit distinct
@@ -35,24 +47,29 @@ __device__ __forceinline__ int swz(int row, int col) {
 // unit; the eight warp partials are combined once at the end, in warp order.
 constexpr int kSub = kPage;          // keys per sub-block
 constexpr int kUnit = kAttnUnit;     // keys per unit (one partial per (row, head, unit))
-constexpr int kGroupRows = 2;        // rows per group: G * 2 <= 16 (row, head) pairs, one m16 tile
+constexpr int kGroupRows = 2;        // rows per group: G * 2 <= 16 (row, head) pairs, two n8 tiles
 constexpr int kPairs = 16;
+// the cp.async kernel's groups: G * 4 <= 32 pairs, four n8 tiles (each pair's
+// arithmetic is the same whatever the group; larger groups give each warp more
+// independent accumulation chains and read each key block once per four rows)
+constexpr int kWideGroupRows = 4;
+constexpr int kWidePairs = 32;
 // combine scratch per pair: the warps' outputs, maxima, sums and weights, and M
 constexpr int kCombPerPair = kWarps * kHeadDim + 3 * kWarps + 1;
 constexpr int kCombFloats = kCombPerPair * kPairs;  // 16 pairs
-// floats of combine scratch for P pairs
-__host__ __device__ constexpr int comb_floats(int P) { return kCombPerPair * ((P + 7) / 8) * 8; }
+// floats of combine scratch for P pairs (the combine takes at most 16 pairs at a time)
+__host__ __device__ constexpr int comb_floats(int P) { return kCombPerPair * ((((P < 16 ? P : 16) + 7) / 8) * 8); }
 
 struct UnitGeom {
     int u, g;        // unit, KV head
-    int r0, P;       // first row of the group (call-wide index), (row, head) pairs (<= 16)
+    int r0, P;       // first row of the group (call-wide index), (row, head) pairs (<= 32)
     int k0;          // first key of the unit
     int nsub;        // sub-blocks holding keys any row of the group sees (1..4)
     int p_first, p_last;  // positions of the group's first and last rows
 };
 
 // One unit partial by the eight warps (threads 0..255).  q_u: shared address
-// of the queries (16 pairs x 128 bf16, swz layout, pairs past P zero), visible
+// of the queries (8 NP pairs x 128 bf16, swz layout, pairs past P zero), visible
 // to every warp.  comb: comb_floats(P) floats of shared memory.  src provides,
 // for sub-block j: wait(j) (this warp may read the sub-block's keys and
 // values; values past the last visible key are exact zeros), done(j) (this
@@ -65,12 +82,18 @@ struct UnitGeom {
 // side: S^T = K Q^T, then O^T += V^T P^T with P^T moved from the accumulator
 // layout into the operand layout by an in-register transpose (movmatrix).
 // Warp w, per pair and sub-block j, over its 16 keys: scores
-// s = (q . k) log2(e)/sqrt(128) (masked: -inf), m_new = max(m, max s),
-// alpha = 2^(m - m_new), p = 2^(s - m_new), l = l alpha + sum p (the thread's
-// two keys in order, then a fixed shuffle tree over the warp's keys),
-// O = O alpha + P V (hi part, then lo part).  Combine: M = max_w m_w,
+// s = (q . k) log2(e)/sqrt(128) (masked: -inf), x = max s over the 16 keys;
+// if x > m + kLazy the reference max moves: alpha = 2^(m - x), m = x, else
+// alpha = 1; p = 2^(s - m) (<= 2^kLazy); per thread l_t = l_t alpha + (its two
+// keys' p), O = O alpha (skipped when no pair of the warp moved: alpha = 1)
+// + P V (hi part, then lo part); at the end of the unit l = the fixed shuffle
+// tree of the eight l_t of the pair.  Combine: M = max_w m_w,
 // a_w = 2^(m_w - M), L = sum_w l_w a_w, O = sum_w O_w a_w (fused multiply-adds
 // in warp order).  A pair with no visible key keeps m = -inf, l = 0, O = 0.
+// Up to two pair tiles the query fragments stay in registers for the unit;
+// with more they are read from shared memory again at every sub-block (the
+// same values, so the same products), and the combine runs in passes of two
+// pair tiles.
 template <int G, int NP, class Src, class Bar>
 __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const UnitGeom& ug, uint32_t q_u,
                                                 float* comb, Src& src, Bar bar) {
@@ -86,10 +109,12 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
     const int trow = (lane & 7) + (lane >> 4) * 8, tcol = ((lane >> 3) & 1) * 8;  // A (trans): 16 x 16
 
     // Q^T as B fragments: [n tile][k step][2]
-    uint32_t qb[NP][kHeadDim / 16][2];
+    constexpr bool kQRegs = NP <= 2;
+    constexpr int NQ = kQRegs ? NP : 1;
+    uint32_t qb[NQ][kHeadDim / 16][2];
 #pragma unroll
-    for (int nt = 0; nt < NP; ++nt) {
-        {
+    for (int nt = 0; nt < NQ; ++nt) {
+        if (kQRegs) {
 #pragma unroll
             for (int ks = 0; ks < kHeadDim / 16; ks += 2) {
                 uint32_t r[4];
@@ -128,47 +153,67 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
         float st[NP][4];
 #pragma unroll
         for (int nt = 0; nt < NP; ++nt) st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.f;
+        if constexpr (kQRegs) {
 #pragma unroll
-        for (int ks = 0; ks < kHeadDim / 16; ++ks) {
-            uint32_t ak[4];
-            ldsm_x4(ak, src.k(j, warp * 16 + arow, ks * 16 + acol));
+            for (int ks = 0; ks < kHeadDim / 16; ++ks) {
+                uint32_t ak[4];
+                ldsm_x4(ak, src.k(j, warp * 16 + arow, ks * 16 + acol));
 #pragma unroll
-            for (int nt = 0; nt < NP; ++nt)
-                mma16816(st[nt], ak, qb[nt][ks][0], qb[nt][ks][1]);
+                for (int nt = 0; nt < NP; ++nt)
+                    mma16816(st[nt], ak, qb[nt][ks][0], qb[nt][ks][1]);
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < kHeadDim / 16; ks += 2) {
+                uint32_t ak0[4], ak1[4];
+                ldsm_x4(ak0, src.k(j, warp * 16 + arow, ks * 16 + acol));
+                ldsm_x4(ak1, src.k(j, warp * 16 + arow, (ks + 1) * 16 + acol));
+#pragma unroll
+                for (int nt = 0; nt < NP; ++nt) {
+                    uint32_t r[4];  // k steps ks and ks + 1 of pair tile nt
+                    ldsm_x4(r, q_u + 2u * swz(nt * 8 + (lane & 7), ks * 16 + (lane >> 3) * 8));
+                    mma16816(st[nt], ak0, r[0], r[1]);
+                    mma16816(st[nt], ak1, r[2], r[3]);
+                }
+            }
         }
-        // ---- per pair: running max, weights, running sums; P^T operands ----
+        // ---- per pair: reference max, weights, running sums; P^T operands ----
+        // every row of the group sees every key of the sub-block: no masking
+        const bool full_vis = kj + kSub - 1 <= ug.p_first;
         uint32_t pbh[NP][2], pbl[NP][2];  // [pair tile][keys 0-7 / 8-15]
 #pragma unroll
         for (int nt = 0; nt < NP; ++nt) {
             float alpha[2], pe[2][2];  // pe[key half][pair e]
+            bool moved = false;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 float mx = -INFINITY;
 #pragma unroll
                 for (int hk = 0; hk < 2; ++hk) {
-                    const int t = warp * 16 + gq + hk * 8;
-                    const bool vis = t < nv && kj + t <= pos_p[nt][e];
                     float& v = st[nt][hk * 2 + e];
-                    v = vis ? v * kScale : -INFINITY;
+                    if (full_vis) {
+                        v *= kScale;
+                    } else {
+                        const int t = warp * 16 + gq + hk * 8;
+                        const bool vis = t < nv && kj + t <= pos_p[nt][e];
+                        v = vis ? v * kScale : -INFINITY;
+                    }
                     mx = fmaxf(mx, v);
                 }
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float m_new = fmaxf(m_w[nt][e], mx);
-                const bool none = m_new == -INFINITY;
-                alpha[e] = none ? 1.f : exp2f(m_w[nt][e] - m_new);
-                m_w[nt][e] = m_new;
-                float l = 0.f;
-#pragma unroll
-                for (int hk = 0; hk < 2; ++hk) {
-                    pe[hk][e] = none ? 0.f : exp2f(st[nt][hk * 2 + e] - m_new);
-                    l += pe[hk][e];
+                alpha[e] = 1.f;
+                if (mx > m_w[nt][e] + kLazy) {  // also the first visible key (m = -inf)
+                    alpha[e] = exp2_approx(m_w[nt][e] - mx);
+                    m_w[nt][e] = mx;
+                    moved = true;
                 }
-                l += __shfl_xor_sync(0xffffffffu, l, 4);
-                l += __shfl_xor_sync(0xffffffffu, l, 8);
-                l += __shfl_xor_sync(0xffffffffu, l, 16);
-                l_w[nt][e] = l_w[nt][e] * alpha[e] + l;
+                const float m = m_w[nt][e];
+#pragma unroll
+                for (int hk = 0; hk < 2; ++hk)
+                    pe[hk][e] = m == -INFINITY ? 0.f : exp2_approx(st[nt][hk * 2 + e] - m);
+                l_w[nt][e] = fmaf(l_w[nt][e], alpha[e], pe[0][e] + pe[1][e]);
             }
 #pragma unroll
             for (int hk = 0; hk < 2; ++hk) {
@@ -176,12 +221,14 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
                 pbh[nt][hk] = movmatrix_t(pack_bf16(h0, h1));
                 pbl[nt][hk] = movmatrix_t(pack_bf16(rn(pe[hk][0] - bf(h0)), rn(pe[hk][1] - bf(h1))));
             }
+            if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-            for (int dt = 0; dt < kHeadDim / 16; ++dt) {
-                ot[dt][nt][0] *= alpha[0];
-                ot[dt][nt][1] *= alpha[1];
-                ot[dt][nt][2] *= alpha[0];
-                ot[dt][nt][3] *= alpha[1];
+                for (int dt = 0; dt < kHeadDim / 16; ++dt) {
+                    ot[dt][nt][0] *= alpha[0];
+                    ot[dt][nt][1] *= alpha[1];
+                    ot[dt][nt][2] *= alpha[0];
+                    ot[dt][nt][3] *= alpha[1];
+                }
             }
         }
         // ---- O^T += V^T P^T over this warp's 16 keys: 8 dim tiles ----
@@ -198,75 +245,101 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
         src.done(j);
     }
 
-    // ---- combine the eight warp partials (warp order) ----
-    constexpr int PS = NP * 8;                          // pair stride of the scratch
+    // each pair's sum over the warp's keys: the eight threads' sums by a fixed tree
+#pragma unroll
+    for (int nt = 0; nt < NP; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float l = l_w[nt][e];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            l_w[nt][e] = l;
+        }
+    // ---- combine the eight warp partials (warp order), two pair tiles a pass ----
+    constexpr int CT = NP < 2 ? NP : 2;                 // pair tiles per pass
+    constexpr int PS = CT * 8;                          // pair stride of the scratch
     float* co = comb;                                   // [warp][pair][dim]
     float* cm = comb + kWarps * PS * kHeadDim;          // [warp][pair]
     float* cl = cm + kWarps * PS;
     float* cw = cl + kWarps * PS;                       // [warp][pair]: 2^(m_w - M)
     float* cM = cw + kWarps * PS;                       // [pair]: M
 #pragma unroll
-    for (int nt = 0; nt < NP; ++nt) {
+    for (int c0 = 0; c0 < NP; c0 += CT) {
+        if (c0 > 0) bar();  // the previous pass is done with the scratch
 #pragma unroll
-        for (int dt = 0; dt < kHeadDim / 16; ++dt)
+        for (int nt = c0; nt < (c0 + CT < NP ? c0 + CT : NP); ++nt) {
+            const int lt = nt - c0;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int p = nt * 8 + 2 * tig + e;
-                co[((size_t)warp * PS + p) * kHeadDim + dt * 16 + gq] = ot[dt][nt][e];
-                co[((size_t)warp * PS + p) * kHeadDim + dt * 16 + gq + 8] = ot[dt][nt][2 + e];
-            }
-        if (gq == 0) {
+            for (int dt = 0; dt < kHeadDim / 16; ++dt)
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                cm[warp * PS + nt * 8 + 2 * tig + e] = m_w[nt][e];
-                cl[warp * PS + nt * 8 + 2 * tig + e] = l_w[nt][e];
+                for (int e = 0; e < 2; ++e) {
+                    const int p = lt * 8 + 2 * tig + e;
+                    co[((size_t)warp * PS + p) * kHeadDim + dt * 16 + gq] = ot[dt][nt][e];
+                    co[((size_t)warp * PS + p) * kHeadDim + dt * 16 + gq + 8] = ot[dt][nt][2 + e];
+                }
+            if (gq == 0) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    cm[warp * PS + lt * 8 + 2 * tig + e] = m_w[nt][e];
+                    cl[warp * PS + lt * 8 + 2 * tig + e] = l_w[nt][e];
+                }
             }
         }
-    }
-    bar();
-    // one thread per (warp, pair): M = max_w m_w and the weight a_w = 2^(m_w - M)
-    if (tid < kWarps * PS) {
-        const int w = tid / PS, p = tid % PS;
-        if (p < P) {
-            float M = cm[p];
+        bar();
+        const int PP = min(PS, P - c0 * 8);  // pairs of this pass
+        // one thread per (warp, pair): M = max_w m_w and the weight a_w = 2^(m_w - M)
+        if (tid < kWarps * PS) {
+            const int w = tid / PS, p = tid % PS;
+            if (p < PP) {
+                float M = cm[p];
 #pragma unroll
-            for (int v = 1; v < kWarps; ++v) M = fmaxf(M, cm[v * PS + p]);
-            const float mw = cm[w * PS + p];
-            cw[w * PS + p] = (M == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - M);
-            if (w == 0) cM[p] = M;
+                for (int v = 1; v < kWarps; ++v) M = fmaxf(M, cm[v * PS + p]);
+                const float mw = cm[w * PS + p];
+                cw[w * PS + p] = (M == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - M);
+                if (w == 0) cM[p] = M;
+            }
         }
-    }
-    bar();
-    const int d = tid & (kHeadDim - 1);
-    for (int p = tid >> 7; p < P; p += 2) {
-        const float M = cM[p];
-        float O = 0.f, L = 0.f;
-        if (M != -INFINITY) {
+        bar();
+        const int d = tid & (kHeadDim - 1);
+        for (int p = tid >> 7; p < PP; p += 2) {
+            const float M = cM[p];
+            float O = 0.f, L = 0.f;
+            if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) O = fmaf(co[((size_t)w * PS + p) * kHeadDim + d], cw[w * PS + p], O);
+                for (int w = 0; w < kWarps; ++w) O = fmaf(co[((size_t)w * PS + p) * kHeadDim + d], cw[w * PS + p], O);
+                if (d == 0) {
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) L = fmaf(cl[w * PS + p], cw[w * PS + p], L);
+                }
+            }
+            const int pg = c0 * 8 + p;
+            const int row = ug.r0 + pg / G, head = ug.g * G + pg % G;
+            const size_t idx = ((size_t)row * a.n_q + head) * a.max_blocks + ug.u;
+            a.po[idx * kHeadDim + d] = O;
             if (d == 0) {
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) L = fmaf(cl[w * PS + p], cw[w * PS + p], L);
+                a.pm[idx] = M;
+                a.pl[idx] = L;
             }
-        }
-        const int row = ug.r0 + p / G, head = ug.g * G + p % G;
-        const size_t idx = ((size_t)row * a.n_q + head) * a.max_blocks + ug.u;
-        a.po[idx * kHeadDim + d] = O;
-        if (d == 0) {
-            a.pm[idx] = M;
-            a.pl[idx] = L;
         }
     }
     bar();  // the combine scratch and the queries may be reused
 }
 
-template <int G, class Src, class Bar>
+// The unit partial for P pairs; MAXNP (2 or 4) bounds the pair tiles the
+// caller's groups can need, so kernels of two-row groups compile no wider path.
+template <int G, int MAXNP = 2, class Src, class Bar>
 __device__ __forceinline__ void unit_partial(const AttnDecodeArgs& a, const UnitGeom& ug, uint32_t q_u, float* comb,
                                              Src& src, Bar bar) {
+    static_assert(MAXNP == 2 || MAXNP == 4, "two or four pair tiles");
     if (ug.P <= 8)
         unit_partial_np<G, 1>(a, ug, q_u, comb, src, bar);
-    else
+    else if (MAXNP == 2 || ug.P <= 16)
         unit_partial_np<G, 2>(a, ug, q_u, comb, src, bar);
+    else if (ug.P <= 24)
+        unit_partial_np<G, MAXNP == 2 ? 2 : 3>(a, ug, q_u, comb, src, bar);
+    else
+        unit_partial_np<G, MAXNP>(a, ug, q_u, comb, src, bar);
 }
 
 // Merge of (row, head) over its units: M = max_u m_u; the units are cut into

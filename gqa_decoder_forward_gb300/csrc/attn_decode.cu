@@ -4,7 +4,7 @@
 // absolute positions").
 //
 // Pass 1 (attn_block_kernel): one CTA per (unit u of 512 positions, KV head g,
-// group of <= 2 rows of one stream).  The unit's four 128-key sub-blocks of
+// group of <= 4 rows of one stream).  The unit's four 128-key sub-blocks of
 // head g stream through two shared-memory buffers (cp.async), one computed
 // while the next lands.  The G = n_q/n_kv query heads of the group's rows form
 // the M dimension of tensor-core products (mma.sync m16n8k16, bf16 in, fp32
@@ -46,16 +46,16 @@ namespace tfl {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRB = attn::kGroupRows;  // rows per CTA
+constexpr int kRB = attn::kWideGroupRows;  // rows per CTA of attn_block_kernel
 constexpr int kSub = attn::kSub;
 constexpr int kUnit = attn::kUnit;
 using attn::swz;
 
-// 202,304 bytes (one CTA per SM): queries, two buffers of one sub-block's
+// 206,400 bytes (one CTA per SM): queries, two buffers of one sub-block's
 // keys and values each (sub-block j+1 streams in while j is computed), and the
-// scratch that combines the eight warp partials.
+// scratch that combines the eight warp partials (16 pairs at a time).
 struct Smem {
-    bf16 q[attn::kPairs * kHeadDim];     // 4 KB
+    bf16 q[attn::kWidePairs * kHeadDim];  // 8 KB
     bf16 k[2][kSub * kHeadDim];          // 2 x 32 KB
     bf16 v[2][kSub * kHeadDim];          // 2 x 32 KB
     float comb[attn::kCombFloats];       // 65 KB
@@ -65,15 +65,16 @@ using wm::cp_async16_zfill;
 using wm::cp_async_commit;
 using wm::cp_async_wait;
 
-// Locates row group z: stream s, first row (global index) r0, row count nr.
-__device__ __forceinline__ bool find_group(const RowMap& m, int z, int& s, int& r0, int& nr) {
+// Locates row group z of groups of rb rows: stream s, first row (global
+// index) r0, row count nr.
+__device__ __forceinline__ bool find_group(const RowMap& m, int z, int rb, int& s, int& r0, int& nr) {
     for (int t = 0; t < m.n_streams; ++t) {
         int rows = m.row_start[t + 1] - m.row_start[t];
-        int ng = (rows + kRB - 1) / kRB;
+        int ng = (rows + rb - 1) / rb;
         if (z < ng) {
             s = t;
-            r0 = m.row_start[t] + z * kRB;
-            nr = min(kRB, rows - z * kRB);
+            r0 = m.row_start[t] + z * rb;
+            nr = min(rb, rows - z * rb);
             return true;
         }
         z -= ng;
@@ -134,14 +135,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_block_kernel(const __grid_co
     Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
 
     int s, r0, nr;
-    if (!find_group(a.rows, blockIdx.z, s, r0, nr)) return;
+    if (!find_group(a.rows, blockIdx.z, kRB, s, r0, nr)) return;
     const int u = blockIdx.x, g = blockIdx.y;
     const int p_first = a.rows.pos0[s] + (r0 - a.rows.row_start[s]);
     const int p_last = p_first + nr - 1;
     const int k0 = u * kUnit;
     if (k0 > p_last) return;
     const int tid = threadIdx.x;
-    const int P = nr * G;  // (row, head) pairs, at most 16
+    const int P = nr * G;  // (row, head) pairs, at most 32
 
     CpSrc src;
     src.sm = &sm;
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_block_kernel(const __grid_co
         if (src.nsub > 1) src.load(1);
     }
     // queries (bf16, unscaled); pairs past P are zero
-    for (int i = tid; i < attn::kPairs * 16; i += kThreads) {
+    for (int i = tid; i < attn::kWidePairs * 16; i += kThreads) {
         const int p = i >> 4, c = i & 15;
         uint4 val = make_uint4(0u, 0u, 0u, 0u);
         if (p < P) {
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_block_kernel(const __grid_co
     ug.nsub = src.nsub;
     ug.p_first = p_first;
     ug.p_last = p_last;
-    attn::unit_partial<G>(a, ug, smem_u32(sm.q), sm.comb, src, [] { __syncthreads(); });
+    attn::unit_partial<G, 4>(a, ug, smem_u32(sm.q), sm.comb, src, [] { __syncthreads(); });
 }
 
 // ---- TMA-fed variant -------------------------------------------------------------
@@ -220,7 +221,7 @@ __device__ __forceinline__ bool item_at(const AttnDecodeArgs& a, int w, int nblk
     it.u = w % nblk;
     const int rest = w / nblk;
     it.g = rest % a.n_kv;
-    if (!find_group(a.rows, rest / a.n_kv, it.s, it.r0, it.nr)) return false;
+    if (!find_group(a.rows, rest / a.n_kv, attn::kGroupRows, it.s, it.r0, it.nr)) return false;
     it.p_first = a.rows.pos0[it.s] + (it.r0 - a.rows.row_start[it.s]);
     it.p_last = it.p_first + it.nr - 1;
     it.k0 = it.u * kUnit;
@@ -464,11 +465,12 @@ cudaError_t init_attn_decode_tma() {
     return cudaFuncSetAttribute(attn_block_tma_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
 }
 
-int attn_decode_blocks(const AttnDecodeArgs& a, int* groups) {
+// Key blocks of the call; *groups = row groups of rb rows.
+int attn_decode_blocks(const AttnDecodeArgs& a, int rb, int* groups) {
     int g = 0, max_pos = 0;
     for (int s = 0; s < a.rows.n_streams; ++s) {
         int rows = a.rows.row_start[s + 1] - a.rows.row_start[s];
-        g += (rows + kRB - 1) / kRB;
+        g += (rows + rb - 1) / rb;
         max_pos = max(max_pos, a.rows.pos0[s] + rows - 1);
     }
     *groups = g;
@@ -479,7 +481,7 @@ cudaError_t launch_attn_block(const AttnDecodeArgs& a, cudaStream_t st, bool pdl
     const int G = a.n_q / a.n_kv;
     if ((G != 7 && G != 8) || a.n_q % a.n_kv != 0) return cudaErrorInvalidValue;
     int groups = 0;
-    const int nblk = attn_decode_blocks(a, &groups);
+    const int nblk = attn_decode_blocks(a, kRB, &groups);
     if (nblk > a.max_blocks) return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -501,7 +503,7 @@ cudaError_t launch_attn_block_tma(const AttnDecodeArgs& a, const KvMaps& maps, i
     for (int s = 0; s < a.rows.n_streams; ++s)  // the combine scratch holds one row's pairs
         if (a.rows.row_start[s + 1] - a.rows.row_start[s] != 1) return cudaErrorInvalidValue;
     int groups = 0;
-    const int nblk = attn_decode_blocks(a, &groups);
+    const int nblk = attn_decode_blocks(a, attn::kGroupRows, &groups);
     if (nblk > a.max_blocks) return cudaErrorInvalidValue;
     // one CTA per SM of the model's device at most (the shared memory holds one)
     const int W = nblk * a.n_kv * groups;  // work items
