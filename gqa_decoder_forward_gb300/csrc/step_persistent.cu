@@ -49,11 +49,12 @@ constexpr int kMaxDepth = 8;
 __host__ __device__ constexpr int ring_depth(int) { return 8; }
 __host__ __device__ constexpr int xs_bytes(int rows) { return rows * 22016 * 2; }  // down-projection lines
 constexpr int kStage = kABytes;                       // 16 KB: one weight stage or one K/V tile
-// the activation space also holds the attention's queries and combine scratch,
-// and the merge's scratch and staged partials
-static_assert(attn::kPairs * kHeadDim * 2 + attn::comb_floats(attn::kGroupRows * 8) * 4 <= xs_bytes(kStepMaxRows),
+// the activation space also holds the attention's two query buffers and
+// combine scratch, and the merge's scratch and staged partials
+constexpr int kQBytes = attn::kPairs * kHeadDim * 2;  // one unit's queries
+static_assert(2 * kQBytes + attn::comb_floats(attn::kGroupRows * 8) * 4 <= xs_bytes(kStepMaxRows),
               "attention scratch exceeds the activation space");
-static_assert(attn::comb_floats(8) * 4 + attn::kPairs * kHeadDim * 2 <= xs_bytes(1), "one-row attention scratch");
+static_assert(2 * kQBytes + attn::comb_floats(8) * 4 <= xs_bytes(1), "one-row attention scratch");
 static_assert(8192 + attn::kMergeStageFloats * 4 <= xs_bytes(1), "merge scratch exceeds the activation space");
 constexpr int kRedBytes = kConsumerWarps * 4 * 32 * 4;
 constexpr int kPhasesPerLayer = 6;
@@ -345,28 +346,30 @@ struct RingSrc {
     }
 };
 
+// Copies the queries of unit x's (row, head) pairs into the swizzled query
+// buffer at q_u (pairs past the unit's are zero-filled), one 16-byte chunk per
+// consumer thread, as an asynchronous copy group.
 template <int GQ>
-__device__ __forceinline__ void attention_unit(const StepArgs& a, const AttnDecodeArgs& at, const Unit& x,
-                                               unsigned char* ring, unsigned char* xs, uint64_t* full, uint64_t* empty,
-                                               RingPos rp, volatile int* s_abort) {
-    const int tid = threadIdx.x;
-    const ConsumerBar bar;
-    const int P = x.nr * GQ;
-    const uint32_t q_u = smem_u32(xs);
-    float* comb = reinterpret_cast<float*>(xs + attn::kPairs * kHeadDim * 2);
-    // queries of the group's (row, head) pairs; pairs past P are zero
-    for (int i = tid; i < attn::kPairs * 16; i += kConsumerWarps * 32) {
-        const int p = i >> 4, c = i & 15;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (p < P) {
-            const int row = x.r0 + p / GQ, head = x.g * GQ + p % GQ;
-            val = *reinterpret_cast<const uint4*>(a.q + (size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + c * 8);
-        }
-        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(q_u + 2u * attn::swz(p, c * 8)), "r"(val.x),
-                     "r"(val.y), "r"(val.z), "r"(val.w)
-                     : "memory");
+__device__ __forceinline__ void load_queries(const StepArgs& a, const Unit& x, uint32_t q_u) {
+    static_assert(attn::kPairs * 16 == kConsumerWarps * 32, "one query chunk per consumer thread");
+    const int p = threadIdx.x >> 4, c = threadIdx.x & 15, P = x.nr * GQ;
+    const bf16* src = a.q;
+    if (p < P) {
+        const int row = x.r0 + p / GQ, head = x.g * GQ + p % GQ;
+        src = a.q + (size_t)row * a.n_q * kHeadDim + (size_t)head * kHeadDim + c * 8;
     }
-    bar();
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(q_u + 2u * attn::swz(p, c * 8)), "l"(src),
+                 "r"(p < P ? 16 : 0)
+                 : "memory");
+    wm::cp_async_commit();
+}
+
+// The partial of unit x with its queries already in the buffer at q_u.
+template <int GQ>
+__device__ __forceinline__ void attention_unit(const StepArgs& a, const AttnDecodeArgs& at, const Unit& x, uint32_t q_u,
+                                               float* comb, unsigned char* ring, uint64_t* full, uint64_t* empty,
+                                               RingPos rp, volatile int* s_abort) {
+    const ConsumerBar bar;
     RingSrc src;
     src.ring = ring;
     src.full = full;
@@ -380,13 +383,30 @@ __device__ __forceinline__ void attention_unit(const StepArgs& a, const AttnDeco
     ug.u = x.b;
     ug.g = x.g;
     ug.r0 = x.r0;
-    ug.P = P;
+    ug.P = x.nr * GQ;
     ug.k0 = x.k0;
     ug.nsub = x.nsub;
     ug.p_first = x.p_first;
     ug.p_last = x.p_last;
     attn::unit_partial<GQ>(at, ug, q_u, comb, src, bar);
 }
+
+// This CTA's attention units in order: those reading only blocks written by
+// earlier steps (pass 0), then those reaching this step's rows (pass 1).
+struct UnitWalk {
+    int pass, u;
+    __device__ __forceinline__ bool next(const StepArgs& a, int nblk, int units, Unit& x) {
+        for (;;) {
+            u += gridDim.x;
+            if (u >= units) {
+                if (++pass == 2) return false;
+                u = blockIdx.x;
+            }
+            if (u < units && attn_unit(a, u, nblk, x) && (int)x.late == pass) return true;
+            if (u >= units) return false;
+        }
+    }
+};
 
 __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char* xs, float* red, float* red_norm,
                           uint64_t* full, uint64_t* empty, volatile int* s_abort) {
@@ -456,18 +476,36 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
             matvec(l, PH_QKV, hrow, a.norms[2 * l]);
         }
         if (!grid_barrier()) return;
-        // attention block partials: blocks written by earlier steps, then this step's
-        for (int pass = 0; pass < 2; ++pass)
-            for (int u = blockIdx.x; u < units; u += G) {
-                Unit x;
-                if (!attn_unit(a, u, nblk, x) || (int)x.late != pass) continue;
-                bar();  // the previous unit is done with the queries and weights
-                if (GQ == 7)
-                    attention_unit<7>(a, at, x, ring, xs, full, empty, rp, s_abort);
-                else
-                    attention_unit<8>(a, at, x, ring, xs, full, empty, rp, s_abort);
-                for (int j = 0; j < 4 * x.nsub; ++j) rp.advance();
+        // attention block partials: blocks written by earlier steps, then this
+        // step's; the next unit's queries are copied while this one runs
+        {
+            float* comb = reinterpret_cast<float*>(xs + 2 * kQBytes);
+            UnitWalk walk{0, (int)blockIdx.x - G};
+            Unit cur, nxt;
+            bool have = walk.next(a, nblk, units, cur);
+            int qb = 0;
+            if (have) {
+                if (GQ == 7) load_queries<7>(a, cur, xs_u); else load_queries<8>(a, cur, xs_u);
+                wm::cp_async_wait_all();
             }
+            while (have) {
+                const bool have_next = walk.next(a, nblk, units, nxt);
+                bar();  // the queries of cur are in place; the previous unit is done with the scratch
+                const uint32_t q_cur = xs_u + qb * kQBytes, q_nxt = xs_u + (qb ^ 1) * kQBytes;
+                if (have_next) {
+                    if (GQ == 7) load_queries<7>(a, nxt, q_nxt); else load_queries<8>(a, nxt, q_nxt);
+                }
+                if (GQ == 7)
+                    attention_unit<7>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort);
+                else
+                    attention_unit<8>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort);
+                for (int j = 0; j < 4 * cur.nsub; ++j) rp.advance();
+                wm::cp_async_wait_all();
+                cur = nxt;
+                have = have_next;
+                qb ^= 1;
+            }
+        }
         if (!grid_barrier()) return;
         // merge: one (row, head) at a time
         {
