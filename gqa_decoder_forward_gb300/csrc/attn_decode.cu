@@ -428,7 +428,8 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
             ug.nsub = it.nsub;
             ug.p_first = it.p_first;
             ug.p_last = it.p_last;
-            attn::unit_partial<G>(a, ug, smem_u32(qbuf + qb * attn::kPairs * kHeadDim), comb, src, bar);
+            // one-row items: at most 8 (row, head) pairs, one pair tile
+            attn::unit_partial_np<G, 1>(a, ug, smem_u32(qbuf + qb * attn::kPairs * kHeadDim), comb, src, bar);
             if (wn >= W) break;
             for (int i = 0; i < 4 * it.nsub; ++i) first.advance();
             it = nx;

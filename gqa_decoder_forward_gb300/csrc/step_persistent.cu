@@ -365,7 +365,8 @@ __device__ __forceinline__ void load_queries(const StepArgs& a, const Unit& x, u
 }
 
 // The partial of unit x with its queries already in the buffer at q_u.
-template <int GQ>
+// MAXNP: pair tiles the step's units can need (1 when every stream has one row).
+template <int GQ, int MAXNP>
 __device__ __forceinline__ void attention_unit(const StepArgs& a, const AttnDecodeArgs& at, const Unit& x, uint32_t q_u,
                                                float* comb, unsigned char* ring, uint64_t* full, uint64_t* empty,
                                                RingPos rp, volatile int* s_abort) {
@@ -388,7 +389,10 @@ __device__ __forceinline__ void attention_unit(const StepArgs& a, const AttnDeco
     ug.nsub = x.nsub;
     ug.p_first = x.p_first;
     ug.p_last = x.p_last;
-    attn::unit_partial<GQ>(at, ug, q_u, comb, src, bar);
+    if (MAXNP == 1)
+        attn::unit_partial_np<GQ, 1>(at, ug, q_u, comb, src, bar);
+    else
+        attn::unit_partial<GQ>(at, ug, q_u, comb, src, bar);
 }
 
 // This CTA's attention units in order: those reading only blocks written by
@@ -408,6 +412,7 @@ struct UnitWalk {
     }
 };
 
+template <int MAXNP>
 __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char* xs, float* red, float* red_norm,
                           uint64_t* full, uint64_t* empty, volatile int* s_abort) {
     const int tid = threadIdx.x, lane = tid & 31, tig = lane & 3;
@@ -496,9 +501,9 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
                     if (GQ == 7) load_queries<7>(a, nxt, q_nxt); else load_queries<8>(a, nxt, q_nxt);
                 }
                 if (GQ == 7)
-                    attention_unit<7>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort);
+                    attention_unit<7, MAXNP>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort);
                 else
-                    attention_unit<8>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort);
+                    attention_unit<8, MAXNP>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort);
                 for (int j = 0; j < 4 * cur.nsub; ++j) rp.advance();
                 wm::cp_async_wait_all();
                 cur = nxt;
@@ -528,6 +533,9 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
     stamp(1);
 }
 
+// MAXNP = 1: every stream of the step has one row (the attention's items have
+// at most eight (row, head) pairs); 2: a stream has two rows.
+template <int MAXNP>
 __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* ring =
@@ -559,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         }
         return;
     }
-    consumers(a, ring, xs, red, red_norm, full, empty, s_abort);
+    consumers<MAXNP>(a, ring, xs, red, red_norm, full, empty, s_abort);
 }
 
 // The two bounded waits of the step kernel run alone, each on something that
@@ -598,7 +606,10 @@ int step_smem_bytes(int rows) {
 }
 
 cudaError_t init_step_persistent() {
-    return cudaFuncSetAttribute(step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(step_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         std::max(step_smem_bytes(1), step_smem_bytes(2)));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(step_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 std::max(step_smem_bytes(1), step_smem_bytes(2)));
 }
 
@@ -618,7 +629,8 @@ cudaError_t launch_step_persistent(const StepArgs& a, int grid, cudaStream_t st)
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, step_kernel, a);
+    const bool one_row_streams = a.rows.n_rows == a.rows.n_streams;
+    return one_row_streams ? cudaLaunchKernelEx(&cfg, step_kernel<1>, a) : cudaLaunchKernelEx(&cfg, step_kernel<2>, a);
 }
 
 }  // namespace tfl
