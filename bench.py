@@ -222,6 +222,20 @@ def decode_config(args, world):
             "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
+def host_ram_gb() -> float:
+    """Physical memory of this host, GB."""
+    try:
+        return os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES") / 1e9
+    except (ValueError, OSError, AttributeError):
+        return float("nan")
+
+
+def oracle_weight_gb(layers: int) -> float:
+    """Bytes of bf16 weights a whole oracle model of `layers` layers holds, GB."""
+    per_layer = 1_181_773_824
+    return (layers * per_layer + 2 * SHAPE.vocab * SHAPE.hidden * 2) / 1e9
+
+
 def run_reference(args, world, rank):
     """The oracle arm.  A timed step is a bounded sample of the decode step: one
     33B-shaped decoder layer of the oracle (one row at the benchmark's context,
@@ -274,7 +288,11 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_layer * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (random-init weights, seeded KV)",
         "config": decode_config(args, world),
-        "reference_step": f"one of {args.layers} layers per timed step; value extrapolated to the whole step",
+        "reference_step": (f"one of {args.layers} layers per timed step; value extrapolated to the whole step "
+                           f"(a whole {args.layers}-layer oracle step would hold about "
+                           f"{oracle_weight_gb(args.layers):.0f} GB of bf16 weights in host memory; this host has "
+                           f"{host_ram_gb():.0f} GB; sampled per layer so that the run ends within minutes)"),
+        "host_ram_gb": round(host_ram_gb(), 1),
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
