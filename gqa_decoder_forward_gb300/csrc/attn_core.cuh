@@ -68,6 +68,58 @@ struct UnitGeom {
     int p_first, p_last;  // positions of the group's first and last rows
 };
 
+// The second half of the combine of one pass of up to PS pairs (pairs c0 * 8
+// .. c0 * 8 + PP - 1 of the unit), once the eight warps' outputs, maxima and
+// sums are in the scratch (co [warp][pair][dim], cm and cl [warp][pair], pair
+// stride PS): one thread per (warp, pair) takes M = max_w m_w and
+// a_w = 2^(m_w - M) into cw and cM, then thread (pair, dim) folds
+// O = sum_w O_w a_w and L = sum_w l_w a_w in warp order and writes the unit's
+// m_u = M, l_u = L and o_u = O.  Run by T threads (tid = 0..T-1, T >= 8 PS, a
+// multiple of 128); bar() synchronises those T threads.
+template <int G, int PS, int T, class Bar>
+__device__ __forceinline__ void combine_pass(const AttnDecodeArgs& a, int r0, int g, int u, int c0, int PP,
+                                             float* comb, int tid, Bar bar) {
+    static_assert(T % kHeadDim == 0 && T >= kWarps * PS, "combine threads");
+    const float* co = comb;
+    const float* cm = comb + kWarps * PS * kHeadDim;
+    const float* cl = cm + kWarps * PS;
+    float* cw = const_cast<float*>(cl) + kWarps * PS;
+    float* cM = cw + kWarps * PS;
+    if (tid < kWarps * PS) {
+        const int w = tid / PS, p = tid % PS;
+        if (p < PP) {
+            float M = cm[p];
+#pragma unroll
+            for (int v = 1; v < kWarps; ++v) M = fmaxf(M, cm[v * PS + p]);
+            const float mw = cm[w * PS + p];
+            cw[w * PS + p] = (M == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - M);
+            if (w == 0) cM[p] = M;
+        }
+    }
+    bar();
+    const int d = tid & (kHeadDim - 1);
+    for (int p = tid / kHeadDim; p < PP; p += T / kHeadDim) {
+        const float M = cM[p];
+        float O = 0.f, L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) O = fmaf(co[((size_t)w * PS + p) * kHeadDim + d], cw[w * PS + p], O);
+            if (d == 0) {
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) L = fmaf(cl[w * PS + p], cw[w * PS + p], L);
+            }
+        }
+        const int pg = c0 * 8 + p;
+        const int row = r0 + pg / G, head = g * G + pg % G;
+        const size_t idx = ((size_t)row * a.n_q + head) * a.max_blocks + u;
+        a.po[idx * kHeadDim + d] = O;
+        if (d == 0) {
+            a.pm[idx] = M;
+            a.pl[idx] = L;
+        }
+    }
+}
+
 // One unit partial by the eight warps (threads 0..255).  q_u: shared address
 // of the queries (8 NP pairs x 128 bf16, swz layout, pairs past P zero), visible
 // to every warp.  comb: comb_floats(P) floats of shared memory.  src provides,
@@ -93,10 +145,17 @@ struct UnitGeom {
 // Up to two pair tiles the query fragments stay in registers for the unit;
 // with more they are read from shared memory again at every sub-block (the
 // same values, so the same products), and the combine runs in passes of two
-// pair tiles.
-template <int G, int NP, class Src, class Bar>
+// pair tiles.  HANDOFF (at most two pair tiles): the warps only write their
+// outputs, maxima and sums into comb, after pre() (which waits until comb is
+// free), and return; combine_pass, run by other threads once all eight warps
+// have written, finishes the unit.
+struct NoPre {
+    __device__ __forceinline__ void operator()() const {}
+};
+template <int G, int NP, bool HANDOFF = false, class Src, class Bar, class Pre = NoPre>
 __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const UnitGeom& ug, uint32_t q_u,
-                                                float* comb, Src& src, Bar bar) {
+                                                float* comb, Src& src, Bar bar, Pre pre = Pre()) {
+    static_assert(!HANDOFF || NP <= 2, "a hand-off holds one pass");
     using wm::ldsm_x4;
     using wm::ldsm_x4_t;
     using wm::mma16816;
@@ -262,8 +321,7 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
     float* co = comb;                                   // [warp][pair][dim]
     float* cm = comb + kWarps * PS * kHeadDim;          // [warp][pair]
     float* cl = cm + kWarps * PS;
-    float* cw = cl + kWarps * PS;                       // [warp][pair]: 2^(m_w - M)
-    float* cM = cw + kWarps * PS;                       // [pair]: M
+    if (HANDOFF) pre();
 #pragma unroll
     for (int c0 = 0; c0 < NP; c0 += CT) {
         if (c0 > 0) bar();  // the previous pass is done with the scratch
@@ -286,42 +344,9 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
                 }
             }
         }
+        if (HANDOFF) return;
         bar();
-        const int PP = min(PS, P - c0 * 8);  // pairs of this pass
-        // one thread per (warp, pair): M = max_w m_w and the weight a_w = 2^(m_w - M)
-        if (tid < kWarps * PS) {
-            const int w = tid / PS, p = tid % PS;
-            if (p < PP) {
-                float M = cm[p];
-#pragma unroll
-                for (int v = 1; v < kWarps; ++v) M = fmaxf(M, cm[v * PS + p]);
-                const float mw = cm[w * PS + p];
-                cw[w * PS + p] = (M == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - M);
-                if (w == 0) cM[p] = M;
-            }
-        }
-        bar();
-        const int d = tid & (kHeadDim - 1);
-        for (int p = tid >> 7; p < PP; p += 2) {
-            const float M = cM[p];
-            float O = 0.f, L = 0.f;
-            if (M != -INFINITY) {
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) O = fmaf(co[((size_t)w * PS + p) * kHeadDim + d], cw[w * PS + p], O);
-                if (d == 0) {
-#pragma unroll
-                    for (int w = 0; w < kWarps; ++w) L = fmaf(cl[w * PS + p], cw[w * PS + p], L);
-                }
-            }
-            const int pg = c0 * 8 + p;
-            const int row = ug.r0 + pg / G, head = ug.g * G + pg % G;
-            const size_t idx = ((size_t)row * a.n_q + head) * a.max_blocks + ug.u;
-            a.po[idx * kHeadDim + d] = O;
-            if (d == 0) {
-                a.pm[idx] = M;
-                a.pl[idx] = L;
-            }
-        }
+        combine_pass<G, PS, kWarps * 32>(a, ug.r0, ug.g, ug.u, c0, min(PS, P - c0 * 8), comb, tid, bar);
     }
     bar();  // the combine scratch and the queries may be reused
 }

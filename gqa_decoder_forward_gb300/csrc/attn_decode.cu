@@ -15,9 +15,10 @@
 // attn_block_tma_kernel computes the same partials with at most one persistent
 // CTA per SM walking the (unit, KV head, row group) items in a fixed stride: a
 // producer warp streams each item's sub-blocks as 16 KB TMA boxes (keys or
-// values, 64 dims, 128-byte swizzle) through an 8-stage ring, each warp
-// releases a stage once it has read its keys there, and the next item's
-// queries are copied while the warp partials combine.
+// values, 64 dims, 128-byte swizzle) through a 9-stage ring, each compute warp
+// releases a stage once it has read its keys there, the next item's queries
+// are copied during the last sub-block, and the eight warp partials of each
+// unit go to a separate combine warpgroup through two shared buffers.
 // Pass 2 (attn_merge_kernel): per (row, head), M = max_u m_u, then
 // L = sum_u l_u e^(m_u - M) and O = sum_u o_u e^(m_u - M) in unit order,
 // out = bf16(O / L).
@@ -196,19 +197,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_block_kernel(const __grid_co
 
 // ---- TMA-fed variant -------------------------------------------------------------
 
+// Four warpgroups: warps 0-7 compute the unit partials, warps 8-11 combine
+// them, warp 12 is the TMA producer (13-15 idle).  The compute warps hand each
+// unit's eight warp partials to the combine warps through a shared buffer and
+// go on to the next unit (they wait for the buffer only when they are about to
+// write the next unit's partials, a unit later), so the combine and its
+// barriers no longer stall the stream.  setmaxnreg moves registers from the
+// producer and combine warpgroups to the compute warps.
 constexpr int kTConsumerWarps = 8;
-constexpr int kTThreads = (kTConsumerWarps + 1) * 32;  // + one producer warp
-// One-row streams only: an item has at most 8 (row, head) pairs, so the combine
-// scratch is that of 8 pairs and the shared memory it frees goes to the ring.
+constexpr int kTCombineWarps = 4;
+constexpr int kTThreads = 16 * 32;
+constexpr int kTRegsCompute = 168, kTRegsCombine = 112, kTRegsProducer = 56;
+static_assert(128 * (2 * kTRegsCompute + kTRegsCombine + kTRegsProducer) <= kTThreads * 128,
+              "register split exceeds the launch's registers");
+// One-row streams only: an item has at most 8 (row, head) pairs, so a combine
+// buffer is that of 8 pairs.
 constexpr int kTDepth = 11;                            // ring stages
 constexpr int kTCombFloats = attn::comb_floats(8);
 constexpr int kTStage = kSub * 64 * 2;                 // 16 KB: 128 positions x 64 dims
 constexpr int kTOffQ = kTDepth * kTStage;              // two query buffers (4 KB each)
-constexpr int kTOffComb = kTOffQ + 2 * attn::kPairs * kHeadDim * 2;
-constexpr int kTOffBar = kTOffComb + kTCombFloats * 4;
-constexpr int kTSmem = 1024 + kTOffBar + (2 * kTDepth + 2) * 8;
+constexpr int kTOffComb = kTOffQ + 2 * attn::kPairs * kHeadDim * 2;  // the combine buffer
+constexpr int kTOffGeom = kTOffComb + kTCombFloats * 4;             // its unit's (r0, g, u, P)
+constexpr int kTOffBar = kTOffGeom + 16;
+constexpr int kTSmem = 1024 + kTOffBar + (2 * kTDepth + 2) * 8 + 16;
 static_assert(kSub == kPage, "a sub-block is one cache page");
 static_assert(kTSmem <= 227 * 1024, "shared memory");
+static_assert((kTCombFloats * 4) % 16 == 0, "combine buffer alignment");
 
 // A work item: unit u of KV head g for the group of rows r0 .. r0+nr-1 of stream s.
 struct Item {
@@ -326,6 +340,23 @@ struct TConsumerBar {
     __device__ __forceinline__ void operator()() const { named_barrier(1, kTConsumerWarps * 32); }
 };
 
+// Waits for a hand-off (bounded, like mbar_wait), giving up at once when the
+// abort flag rises.
+__device__ __forceinline__ bool wait_handoff(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < kMbarSpinLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u) {
+            if (*abort) return false;
+            if (global_ns() - t0 > kMbarWaitNs) break;
+        }
+    }
+    atomicOr(status, kStatusDevice);
+    *abort = 1;
+    return false;
+}
+
 template <int G>
 __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __grid_constant__ AttnDecodeArgs a,
                                                                       const __grid_constant__ KvMaps maps, int nblk,
@@ -336,9 +367,12 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(base + kTOffBar);
     uint64_t* empty = full + kTDepth;
-    volatile int* abort = reinterpret_cast<volatile int*>(empty + kTDepth);
+    uint64_t* cfull = empty + kTDepth;  // the combine buffer holds the eight warps' partials
+    uint64_t* cempty = cfull + 1;       // the combine warps are done with it
+    volatile int* abort = reinterpret_cast<volatile int*>(cempty + 1);
     bf16* qbuf = reinterpret_cast<bf16*>(base + kTOffQ);
     float* comb = reinterpret_cast<float*>(base + kTOffComb);
+    int4* geom = reinterpret_cast<int4*>(base + kTOffGeom);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     Item it;
     const int w0 = next_item(a, blockIdx.x, W, nblk, it);
@@ -348,14 +382,17 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kTConsumerWarps);
         }
+        mbar_init(cfull, kTConsumerWarps);
+        mbar_init(cempty, 1);
         *abort = 0;
         mbar_init_fence();
     }
     __syncthreads();
 
-    if (warp == kTConsumerWarps) {
+    if (warp >= kTConsumerWarps + kTCombineWarps) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTRegsProducer));
         // ---- producer: every item's sub-blocks in the consumers' order ----
-        if (lane == 0) {
+        if (warp == kTConsumerWarps + kTCombineWarps && lane == 0) {
             const uint64_t pol = policy_evict_first();
             TRing rp{0, 0u};
             long long issued = 0;
@@ -388,58 +425,91 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
             }
             // after an abort, the copies already issued land before the CTA exits
             if (*abort) drain_ring(full, kTDepth, rp.stage, rp.phase, issued, status);
+        } else {
+            pdl_wait();
+            pdl_trigger();
         }
-    } else {
-        // ---- consumers: the eight warps of attn::unit_partial ----
+        return;
+    }
+    if (warp >= kTConsumerWarps) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTRegsCombine));
+        // ---- combine warps: each unit's warp partials, in the compute order ----
         pdl_wait();
         pdl_trigger();
-        for (int i = tid; i < attn::kPairs * 16; i += kTConsumerWarps * 32) {  // the first item's queries
-            const int p = i >> 4, c = i & 15;
-            uint4 val = make_uint4(0u, 0u, 0u, 0u);
-            if (p < it.nr * G) val = *reinterpret_cast<const uint4*>(q_chunk<G>(a, it, p, c));
-            *reinterpret_cast<uint4*>(&qbuf[swz(p, c * 8)]) = val;
+        const int ct = tid - kTConsumerWarps * 32;
+        auto cbar = [] { named_barrier(2, kTCombineWarps * 32); };
+        uint32_t use = 0u;
+        for (int w = w0; w < W; w = next_item(a, w + gridDim.x, W, nblk, it)) {
+            if (!wait_handoff(cfull, use & 1u, abort, status)) break;
+            const int4 gm = *geom;
+            attn::combine_pass<G, 8, kTCombineWarps * 32>(a, gm.x, gm.y, gm.z, 0, gm.w, comb, ct, cbar);
+            cbar();  // every combine thread is done with the buffer
+            if (ct == 0) mbar_arrive(cempty);
+            ++use;
         }
-        TConsumerBar bar;
-        bar();
-        TRing first{0, 0u};
-        int w = w0, qb = 0;
-        while (!*abort) {
-            Item nx;
-            const int wn = next_item(a, w + gridDim.x, W, nblk, nx);
-            TmaSrc<G> src;
-            src.base = base;
-            src.full = full;
-            src.empty = empty;
-            src.first = first;
-            src.status = status;
-            src.abort = abort;
-            src.k0 = it.k0;
-            src.p_last = it.p_last;
-            src.nsub = it.nsub;
-            src.a = &a;
-            src.nx = wn < W ? &nx : nullptr;
-            src.nq = qbuf + (qb ^ 1) * attn::kPairs * kHeadDim;
-            attn::UnitGeom ug;
-            ug.u = it.u;
-            ug.g = it.g;
-            ug.r0 = it.r0;
-            ug.P = it.nr * G;
-            ug.k0 = it.k0;
-            ug.nsub = it.nsub;
-            ug.p_first = it.p_first;
-            ug.p_last = it.p_last;
-            // one-row items: at most 8 (row, head) pairs, one pair tile
-            attn::unit_partial_np<G, 1>(a, ug, smem_u32(qbuf + qb * attn::kPairs * kHeadDim), comb, src, bar);
-            if (wn >= W) break;
-            for (int i = 0; i < 4 * it.nsub; ++i) first.advance();
-            it = nx;
-            w = wn;
-            qb ^= 1;
-            cp_async_wait<0>();
-            bar();  // the next item's queries
-        }
+        return;
     }
-    __syncthreads();
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTRegsCompute));
+    // ---- compute warps: the eight warps of attn::unit_partial ----
+    pdl_wait();
+    pdl_trigger();
+    for (int i = tid; i < attn::kPairs * 16; i += kTConsumerWarps * 32) {  // the first item's queries
+        const int p = i >> 4, c = i & 15;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (p < it.nr * G) val = *reinterpret_cast<const uint4*>(q_chunk<G>(a, it, p, c));
+        *reinterpret_cast<uint4*>(&qbuf[swz(p, c * 8)]) = val;
+    }
+    TConsumerBar bar;
+    bar();
+    TRing first{0, 0u};
+    int w = w0, qb = 0;
+    uint32_t use = 0u;
+    while (!*abort) {
+        Item nx;
+        const int wn = next_item(a, w + gridDim.x, W, nblk, nx);
+        TmaSrc<G> src;
+        src.base = base;
+        src.full = full;
+        src.empty = empty;
+        src.first = first;
+        src.status = status;
+        src.abort = abort;
+        src.k0 = it.k0;
+        src.p_last = it.p_last;
+        src.nsub = it.nsub;
+        src.a = &a;
+        src.nx = wn < W ? &nx : nullptr;
+        src.nq = qbuf + (qb ^ 1) * attn::kPairs * kHeadDim;
+        attn::UnitGeom ug;
+        ug.u = it.u;
+        ug.g = it.g;
+        ug.r0 = it.r0;
+        ug.P = it.nr * G;
+        ug.k0 = it.k0;
+        ug.nsub = it.nsub;
+        ug.p_first = it.p_first;
+        ug.p_last = it.p_last;
+        // one-row items: at most 8 (row, head) pairs, one pair tile; the
+        // partials are written once the combine warps are done with the
+        // previous unit's
+        attn::unit_partial_np<G, 1, true>(a, ug, smem_u32(qbuf + qb * attn::kPairs * kHeadDim), comb, src, bar,
+                                          [&] {
+                                              if (!*abort && !wait_handoff(cempty, (use & 1u) ^ 1u, abort, status))
+                                                  *abort = 1;
+                                          });
+        if (*abort) break;
+        if (tid == 0) *geom = make_int4(ug.r0, ug.g, ug.u, ug.P);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cfull);
+        ++use;
+        if (wn >= W) break;
+        for (int i = 0; i < 4 * it.nsub; ++i) first.advance();
+        it = nx;
+        w = wn;
+        qb ^= 1;
+        cp_async_wait<0>();
+        bar();  // the next item's queries
+    }
 }
 
 // One CTA of 512 threads (a quarter of the units per 128) per (head, row).
