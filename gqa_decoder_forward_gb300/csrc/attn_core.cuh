@@ -54,8 +54,11 @@ constexpr int kPairs = 16;
 // independent accumulation chains and read each key block once per four rows)
 constexpr int kWideGroupRows = 4;
 constexpr int kWidePairs = 32;
-// combine scratch per pair: the warps' outputs, maxima, sums and weights, and M
-constexpr int kCombPerPair = kWarps * kHeadDim + 3 * kWarps + 1;
+// combine scratch per pair: the warps' outputs, maxima, sums and weights, and M.
+// A warp's output row of a pair takes kCoStride floats (128 + 4: the two pairs a
+// thread writes then fall in different banks)
+constexpr int kCoStride = kHeadDim + 4;
+constexpr int kCombPerPair = kWarps * kCoStride + 3 * kWarps + 1;
 constexpr int kCombFloats = kCombPerPair * kPairs;  // 16 pairs
 // floats of combine scratch for P pairs (the combine takes at most 16 pairs at a time)
 __host__ __device__ constexpr int comb_floats(int P) { return kCombPerPair * ((((P < 16 ? P : 16) + 7) / 8) * 8); }
@@ -70,8 +73,8 @@ struct UnitGeom {
 
 // The second half of the combine of one pass of up to PS pairs (pairs c0 * 8
 // .. c0 * 8 + PP - 1 of the unit), once the eight warps' outputs, maxima and
-// sums are in the scratch (co [warp][pair][dim], cm and cl [warp][pair], pair
-// stride PS): one thread per (warp, pair) takes M = max_w m_w and
+// sums are in the scratch (co [warp][pair][dim] in rows of kCoStride, cm and
+// cl [warp][pair], pair stride PS): one thread per (warp, pair) takes M = max_w m_w and
 // a_w = 2^(m_w - M) into cw and cM, then thread (pair, dim) folds
 // O = sum_w O_w a_w and L = sum_w l_w a_w in warp order and writes the unit's
 // m_u = M, l_u = L and o_u = O.  Run by T threads (tid = 0..T-1, T >= 8 PS, a
@@ -81,7 +84,7 @@ __device__ __forceinline__ void combine_pass(const AttnDecodeArgs& a, int r0, in
                                              float* comb, int tid, Bar bar) {
     static_assert(T % kHeadDim == 0 && T >= kWarps * PS, "combine threads");
     const float* co = comb;
-    const float* cm = comb + kWarps * PS * kHeadDim;
+    const float* cm = comb + kWarps * PS * kCoStride;
     const float* cl = cm + kWarps * PS;
     float* cw = const_cast<float*>(cl) + kWarps * PS;
     float* cM = cw + kWarps * PS;
@@ -103,7 +106,7 @@ __device__ __forceinline__ void combine_pass(const AttnDecodeArgs& a, int r0, in
         float O = 0.f, L = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) O = fmaf(co[((size_t)w * PS + p) * kHeadDim + d], cw[w * PS + p], O);
+            for (int w = 0; w < kWarps; ++w) O = fmaf(co[((size_t)w * PS + p) * kCoStride + d], cw[w * PS + p], O);
             if (d == 0) {
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) L = fmaf(cl[w * PS + p], cw[w * PS + p], L);
@@ -318,8 +321,8 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
     // ---- combine the eight warp partials (warp order), two pair tiles a pass ----
     constexpr int CT = NP < 2 ? NP : 2;                 // pair tiles per pass
     constexpr int PS = CT * 8;                          // pair stride of the scratch
-    float* co = comb;                                   // [warp][pair][dim]
-    float* cm = comb + kWarps * PS * kHeadDim;          // [warp][pair]
+    float* co = comb;                                   // [warp][pair][dim], rows of kCoStride
+    float* cm = comb + kWarps * PS * kCoStride;         // [warp][pair]
     float* cl = cm + kWarps * PS;
     if (HANDOFF) pre();
 #pragma unroll
@@ -333,8 +336,8 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int p = lt * 8 + 2 * tig + e;
-                    co[((size_t)warp * PS + p) * kHeadDim + dt * 16 + gq] = ot[dt][nt][e];
-                    co[((size_t)warp * PS + p) * kHeadDim + dt * 16 + gq + 8] = ot[dt][nt][2 + e];
+                    co[((size_t)warp * PS + p) * kCoStride + dt * 16 + gq] = ot[dt][nt][e];
+                    co[((size_t)warp * PS + p) * kCoStride + dt * 16 + gq + 8] = ot[dt][nt][2 + e];
                 }
             if (gq == 0) {
 #pragma unroll
