@@ -440,7 +440,8 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
         auto cbar = [] { named_barrier(2, kTCombineWarps * 32); };
         uint32_t use = 0u;
         for (int w = w0; w < W; w = next_item(a, w + gridDim.x, W, nblk, it)) {
-            if (!wait_handoff(cfull, use & 1u, abort, status)) break;
+            const bool ok = wait_handoff(cfull, use & 1u, abort, status);
+            if (!named_barrier_and(2, kTCombineWarps * 32, ok)) break;  // every combine thread stops together
             const int4 gm = *geom;
             attn::combine_pass<G, 8, kTCombineWarps * 32>(a, gm.x, gm.y, gm.z, 0, gm.w, comb, ct, cbar);
             cbar();  // every combine thread is done with the buffer
@@ -464,7 +465,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
     TRing first{0, 0u};
     int w = w0, qb = 0;
     uint32_t use = 0u;
-    while (!*abort) {
+    for (;;) {
         Item nx;
         const int wn = next_item(a, w + gridDim.x, W, nblk, nx);
         TmaSrc<G> src;
@@ -497,7 +498,6 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
                                               if (!*abort && !wait_handoff(cempty, (use & 1u) ^ 1u, abort, status))
                                                   *abort = 1;
                                           });
-        if (*abort) break;
         if (tid == 0) *geom = make_int4(ug.r0, ug.g, ug.u, ug.P);
         __syncwarp();
         if (lane == 0) mbar_arrive(cfull);
@@ -508,7 +508,8 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
         w = wn;
         qb ^= 1;
         cp_async_wait<0>();
-        bar();  // the next item's queries
+        // the next item's queries; after an abort every compute thread stops here together
+        if (named_barrier_or(1, kTConsumerWarps * 32, *abort != 0)) break;
     }
 }
 

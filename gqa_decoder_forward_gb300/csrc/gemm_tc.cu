@@ -186,7 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         int buf = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            if (*s_abort || !mbar_wait(&acc_full[buf], acc_phase, a.status)) {
+            // the warp leaves together (its lanes then skip whole-warp tensor-memory loads alike)
+            bool stop = *s_abort != 0;
+            if (!stop) stop = !mbar_wait(&acc_full[buf], acc_phase, a.status);
+            if (__any_sync(0xffffffffu, stop)) {
                 *s_abort = 1;
                 break;
             }

@@ -443,8 +443,9 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
             if (!wait_counter(a, epoch * (unsigned)G)) *s_abort = 1;
         }
         stamp(2 * epoch + 1);
-        bar();
-        return !*s_abort;
+        // every consumer thread takes the same decision (the producer may raise
+        // the flag at any moment)
+        return !named_barrier_or(1, kConsumerWarps * 32, *s_abort != 0);
     };
     auto matvec = [&](int l, int ph, auto row, const bf16* norm_w) {
         const MatvecArgs e = phase_args(a, l, ph);

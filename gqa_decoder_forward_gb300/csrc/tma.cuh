@@ -132,6 +132,35 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// The same barrier returning whether `pred` held for any (or) / every (and)
+// participating thread: a decision all of them share, so that no thread leaves
+// a loop that others stay in (an abort flag read at different moments could
+// otherwise differ between threads).
+__device__ __forceinline__ bool named_barrier_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 // Address of 16-byte chunk c of row r in a tile written by TMA with 128-byte
 // swizzling (rows of 128 bytes, 1024-byte aligned tile): chunks are permuted
 // within each row by XOR with (row mod 8).
