@@ -77,19 +77,19 @@ struct UnitGeom {
 // cl [warp][pair], pair stride PS): one thread per (warp, pair) takes M = max_w m_w and
 // a_w = 2^(m_w - M) into cw and cM, then thread (pair, dim) folds
 // O = sum_w O_w a_w and L = sum_w l_w a_w in warp order and writes the unit's
-// m_u = M, l_u = L and o_u = O.  Run by T threads (tid = 0..T-1, T >= 8 PS, a
-// multiple of 128); bar() synchronises those T threads.
+// m_u = M, l_u = L and o_u = O.  Run by T threads (tid = 0..T-1, T a multiple
+// of 32); bar() synchronises those T threads.
 template <int G, int PS, int T, class Bar>
 __device__ __forceinline__ void combine_pass(const AttnDecodeArgs& a, int r0, int g, int u, int c0, int PP,
                                              float* comb, int tid, Bar bar) {
-    static_assert(T % kHeadDim == 0 && T >= kWarps * PS, "combine threads");
+    static_assert(T % 32 == 0, "combine threads");
     const float* co = comb;
     const float* cm = comb + kWarps * PS * kCoStride;
     const float* cl = cm + kWarps * PS;
     float* cw = const_cast<float*>(cl) + kWarps * PS;
     float* cM = cw + kWarps * PS;
-    if (tid < kWarps * PS) {
-        const int w = tid / PS, p = tid % PS;
+    for (int i = tid; i < kWarps * PS; i += T) {
+        const int w = i / PS, p = i % PS;
         if (p < PP) {
             float M = cm[p];
 #pragma unroll
@@ -100,8 +100,8 @@ __device__ __forceinline__ void combine_pass(const AttnDecodeArgs& a, int r0, in
         }
     }
     bar();
-    const int d = tid & (kHeadDim - 1);
-    for (int p = tid / kHeadDim; p < PP; p += T / kHeadDim) {
+    for (int i = tid; i < PP * kHeadDim; i += T) {  // (pair, dim) = (i / 128, i % 128)
+        const int p = i / kHeadDim, d = i % kHeadDim;
         const float M = cM[p];
         float O = 0.f, L = 0.f;
         if (M != -INFINITY) {
@@ -148,10 +148,10 @@ __device__ __forceinline__ void combine_pass(const AttnDecodeArgs& a, int r0, in
 // Up to two pair tiles the query fragments stay in registers for the unit;
 // with more they are read from shared memory again at every sub-block (the
 // same values, so the same products), and the combine runs in passes of two
-// pair tiles.  HANDOFF (at most two pair tiles): the warps only write their
-// outputs, maxima and sums into comb, after pre() (which waits until comb is
-// free), and return; combine_pass, run by other threads once all eight warps
-// have written, finishes the unit.
+// pair tiles.  pre() runs before the warps write into comb (it may wait until
+// comb is free).  HANDOFF (at most two pair tiles): the warps only write their
+// outputs, maxima and sums into comb and return; combine_pass, run by other
+// threads once all eight warps have written, finishes the unit.
 struct NoPre {
     __device__ __forceinline__ void operator()() const {}
 };
@@ -324,7 +324,7 @@ __device__ __forceinline__ void unit_partial_np(const AttnDecodeArgs& a, const U
     float* co = comb;                                   // [warp][pair][dim], rows of kCoStride
     float* cm = comb + kWarps * PS * kCoStride;         // [warp][pair]
     float* cl = cm + kWarps * PS;
-    if (HANDOFF) pre();
+    pre();
 #pragma unroll
     for (int c0 = 0; c0 < NP; c0 += CT) {
         if (c0 > 0) bar();  // the previous pass is done with the scratch

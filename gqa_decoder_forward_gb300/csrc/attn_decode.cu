@@ -340,23 +340,6 @@ struct TConsumerBar {
     __device__ __forceinline__ void operator()() const { named_barrier(1, kTConsumerWarps * 32); }
 };
 
-// Waits for a hand-off (bounded, like mbar_wait), giving up at once when the
-// abort flag rises.
-__device__ __forceinline__ bool wait_handoff(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_ns();
-    for (uint32_t i = 1; i < kMbarSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0u) {
-            if (*abort) return false;
-            if (global_ns() - t0 > kMbarWaitNs) break;
-        }
-    }
-    atomicOr(status, kStatusDevice);
-    *abort = 1;
-    return false;
-}
-
 template <int G>
 __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __grid_constant__ AttnDecodeArgs a,
                                                                       const __grid_constant__ KvMaps maps, int nblk,
@@ -440,7 +423,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
         auto cbar = [] { named_barrier(2, kTCombineWarps * 32); };
         uint32_t use = 0u;
         for (int w = w0; w < W; w = next_item(a, w + gridDim.x, W, nblk, it)) {
-            const bool ok = wait_handoff(cfull, use & 1u, abort, status);
+            const bool ok = mbar_wait_or_abort(cfull, use & 1u, abort, status);
             if (!named_barrier_and(2, kTCombineWarps * 32, ok)) break;  // every combine thread stops together
             const int4 gm = *geom;
             attn::combine_pass<G, 8, kTCombineWarps * 32>(a, gm.x, gm.y, gm.z, 0, gm.w, comb, ct, cbar);
@@ -495,7 +478,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attn_block_tma_kernel(const __gr
         // previous unit's
         attn::unit_partial_np<G, 1, true>(a, ug, smem_u32(qbuf + qb * attn::kPairs * kHeadDim), comb, src, bar,
                                           [&] {
-                                              if (!*abort && !wait_handoff(cempty, (use & 1u) ^ 1u, abort, status))
+                                              if (!*abort && !mbar_wait_or_abort(cempty, (use & 1u) ^ 1u, abort, status))
                                                   *abort = 1;
                                           });
         if (tid == 0) *geom = make_int4(ug.r0, ug.g, ug.u, ug.P);

@@ -2,8 +2,9 @@
 // embedding, every decoder layer and the final norm + lm_head (the decode
 // loop of pull request #1415, section "How", without a launch per operation).
 //
-// One CTA per SM (cooperative launch, so every CTA is resident), 288 threads:
-// warp 8 is a TMA producer, warps 0..7 consume.  The step is a fixed sequence
+// One CTA per SM (cooperative launch, so every CTA is resident), 384 threads:
+// warp 11 is a TMA producer, warps 0..7 compute, warps 8..10 fold the
+// attention units' warp partials handed to them by the compute warps.  The step is a fixed sequence
 // of phases separated by grid barriers:
 //   per layer: RMSNorm + QKV + RoPE + KV append | attention block partials |
 //              merge | o + residual | RMSNorm + gate/up + SwiGLU | down + residual
@@ -42,7 +43,11 @@ using mvc::kABytes;
 using mvc::kConsumerWarps;
 using mvc::kKbPerStage;
 
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+// warps 0-7 compute, then (steps whose attention units outnumber the CTAs)
+// warps 8-10 combine attention partials, then the producer warp
+constexpr int kCombineWarps = 3;
+__host__ __device__ constexpr int producer_warp(bool combine) { return kConsumerWarps + (combine ? kCombineWarps : 0); }
+__host__ __device__ constexpr int step_threads(bool combine) { return (producer_warp(combine) + 1) * 32; }
 // Ring depth (stages) and activation space by rows.  (One row would leave room
 // for 11 stages; measured, 8 stream as well or better.)
 constexpr int kMaxDepth = 8;
@@ -366,10 +371,12 @@ __device__ __forceinline__ void load_queries(const StepArgs& a, const Unit& x, u
 
 // The partial of unit x with its queries already in the buffer at q_u.
 // MAXNP: pair tiles the step's units can need (1 when every stream has one row).
-template <int GQ, int MAXNP>
+// HANDOFF: the warps leave their partials in comb for the combine warps; pre()
+// runs before they write into comb.
+template <int GQ, int MAXNP, bool HANDOFF, class Pre>
 __device__ __forceinline__ void attention_unit(const StepArgs& a, const AttnDecodeArgs& at, const Unit& x, uint32_t q_u,
                                                float* comb, unsigned char* ring, uint64_t* full, uint64_t* empty,
-                                               RingPos rp, volatile int* s_abort) {
+                                               RingPos rp, volatile int* s_abort, Pre pre) {
     const ConsumerBar bar;
     RingSrc src;
     src.ring = ring;
@@ -389,10 +396,10 @@ __device__ __forceinline__ void attention_unit(const StepArgs& a, const AttnDeco
     ug.nsub = x.nsub;
     ug.p_first = x.p_first;
     ug.p_last = x.p_last;
-    if (MAXNP == 1)
-        attn::unit_partial_np<GQ, 1>(at, ug, q_u, comb, src, bar);
+    if (MAXNP == 1 || ug.P <= 8)
+        attn::unit_partial_np<GQ, 1, HANDOFF>(at, ug, q_u, comb, src, bar, pre);
     else
-        attn::unit_partial<GQ>(at, ug, q_u, comb, src, bar);
+        attn::unit_partial_np<GQ, MAXNP == 1 ? 1 : 2, HANDOFF>(at, ug, q_u, comb, src, bar, pre);
 }
 
 // This CTA's attention units in order: those reading only blocks written by
@@ -412,9 +419,51 @@ struct UnitWalk {
     }
 };
 
+// The combine warps (96 threads): per layer, the partials of every attention
+// unit of this CTA but its last (which the compute warps combine themselves),
+// handed over through comb in the compute order; the same combine_pass
+// arithmetic.  Every wait gives up once the abort flag rises; the three warps
+// leave together.
 template <int MAXNP>
+__device__ void combiners(const StepArgs& a, float* comb, uint64_t* cfull, uint64_t* cempty, const int4* geom,
+                          volatile int* s_abort) {
+    const int ct = threadIdx.x - kConsumerWarps * 32;
+    const int nblk = attn_blocks(a), units = nblk * a.n_kv * attn_groups(a);
+    UnitWalk walk{0, (int)blockIdx.x - (int)gridDim.x};
+    Unit x;
+    int n = 0;
+    while (walk.next(a, nblk, units, x)) ++n;
+    const int handoffs = n > 0 ? n - 1 : 0;
+    auto cbar = [] { named_barrier(2, kCombineWarps * 32); };
+    const bool g7 = a.n_q / a.n_kv == 7;
+    uint32_t use = 0;
+    for (int l = 0; l < a.layers; ++l)
+        for (int k = 0; k < handoffs; ++k) {
+            const bool ok = mbar_wait_or_abort(cfull, use & 1u, s_abort, a.status);
+            if (!named_barrier_and(2, kCombineWarps * 32, ok)) return;
+            const int4 gm = *geom;
+            constexpr int T = kCombineWarps * 32;
+            if (MAXNP == 1 || gm.w <= 8) {
+                if (g7)
+                    attn::combine_pass<7, 8, T>(a.attn, gm.x, gm.y, gm.z, 0, gm.w, comb, ct, cbar);
+                else
+                    attn::combine_pass<8, 8, T>(a.attn, gm.x, gm.y, gm.z, 0, gm.w, comb, ct, cbar);
+            } else {
+                if (g7)
+                    attn::combine_pass<7, 16, T>(a.attn, gm.x, gm.y, gm.z, 0, gm.w, comb, ct, cbar);
+                else
+                    attn::combine_pass<8, 16, T>(a.attn, gm.x, gm.y, gm.z, 0, gm.w, comb, ct, cbar);
+            }
+            cbar();  // every combine thread is done with comb
+            if (ct == 0) mbar_arrive(cempty);
+            ++use;
+        }
+}
+
+template <int MAXNP, bool COMBINE>
 __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char* xs, float* red, float* red_norm,
-                          uint64_t* full, uint64_t* empty, volatile int* s_abort) {
+                          uint64_t* full, uint64_t* empty, uint64_t* cfull, uint64_t* cempty, int4* geom,
+                          volatile int* s_abort) {
     const int tid = threadIdx.x, lane = tid & 31, tig = lane & 3;
     const int R = a.rows.n_rows, G = gridDim.x;
     const int QD = a.n_q * kHeadDim, GQ = a.n_q / a.n_kv;
@@ -422,6 +471,7 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
     const uint32_t ring_u = smem_u32(ring), xs_u = smem_u32(xs);
     RingPos rp{0, 0u, ring_depth(a.rows.n_rows)};
     unsigned epoch = 0;
+    uint32_t use = 0;  // hand-offs to the combine warps so far
     const int nblk = attn_blocks(a), units = nblk * a.n_kv * attn_groups(a);
     const AttnDecodeArgs& at = a.attn;
 
@@ -483,7 +533,9 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
         }
         if (!grid_barrier()) return;
         // attention block partials: blocks written by earlier steps, then this
-        // step's; the next unit's queries are copied while this one runs
+        // step's; the next unit's queries are copied while this one runs; every
+        // unit but the CTA's last hands its partials to the combine warps, the
+        // last is combined here (once the combine warps are done with comb)
         {
             float* comb = reinterpret_cast<float*>(xs + 2 * kQBytes);
             UnitWalk walk{0, (int)blockIdx.x - G};
@@ -501,10 +553,28 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
                 if (have_next) {
                     if (GQ == 7) load_queries<7>(a, nxt, q_nxt); else load_queries<8>(a, nxt, q_nxt);
                 }
-                if (GQ == 7)
-                    attention_unit<7, MAXNP>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort);
-                else
-                    attention_unit<8, MAXNP>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort);
+                auto comb_free = [&] {
+                    if (COMBINE && !*s_abort && !mbar_wait_or_abort(cempty, (use & 1u) ^ 1u, s_abort, a.status))
+                        *s_abort = 1;
+                };
+                if (COMBINE && have_next) {
+                    if (GQ == 7)
+                        attention_unit<7, MAXNP, true>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort,
+                                                       comb_free);
+                    else
+                        attention_unit<8, MAXNP, true>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort,
+                                                       comb_free);
+                    if (tid == 0) *geom = make_int4(cur.r0, cur.g, cur.b, cur.nr * GQ);
+                    __syncwarp();
+                    if ((tid & 31) == 0) mbar_arrive(cfull);
+                    ++use;
+                } else if (GQ == 7) {
+                    attention_unit<7, MAXNP, false>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort,
+                                                    comb_free);
+                } else {
+                    attention_unit<8, MAXNP, false>(a, at, cur, q_cur, comb, ring, full, empty, rp, s_abort,
+                                                    comb_free);
+                }
                 for (int j = 0; j < 4 * cur.nsub; ++j) rp.advance();
                 wm::cp_async_wait_all();
                 cur = nxt;
@@ -536,8 +606,10 @@ __device__ void consumers(const StepArgs& a, unsigned char* ring, unsigned char*
 
 // MAXNP = 1: every stream of the step has one row (the attention's items have
 // at most eight (row, head) pairs); 2: a stream has two rows.
-template <int MAXNP>
-__global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant__ StepArgs a) {
+// COMBINE: the variant with combine warps, for steps whose attention units
+// outnumber the CTAs (each CTA then runs several units a layer).
+template <int MAXNP, bool COMBINE>
+__global__ void __launch_bounds__(step_threads(COMBINE), 1) step_kernel(const __grid_constant__ StepArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* ring =
         reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -547,18 +619,27 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
     float* red_norm = red + kRedBytes / 4;
     uint64_t* full = reinterpret_cast<uint64_t*>(red_norm + 8 * kStepMaxRows);
     uint64_t* empty = full + kMaxDepth;
-    volatile int* s_abort = reinterpret_cast<volatile int*>(empty + kMaxDepth);
+    uint64_t* cfull = empty + kMaxDepth;  // comb holds a unit's warp partials
+    uint64_t* cempty = cfull + 1;         // the combine warps are done with comb
+    int4* geom = reinterpret_cast<int4*>(cempty + 1);  // the handed-over unit: (r0, g, unit, pairs)
+    volatile int* s_abort = reinterpret_cast<volatile int*>(geom + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < depth; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
+        mbar_init(cfull, kConsumerWarps);
+        mbar_init(cempty, 1);
         *s_abort = 0;
         mbar_init_fence();
     }
     __syncthreads();
-    if (warp == kConsumerWarps) {
+    if (COMBINE && warp >= kConsumerWarps && warp < producer_warp(COMBINE)) {
+        combiners<MAXNP>(a, reinterpret_cast<float*>(xs + 2 * kQBytes), cfull, cempty, geom, s_abort);
+        return;
+    }
+    if (warp == producer_warp(COMBINE)) {
         if (lane == 0) {
             RingPos rp{0, 0u, depth};
             long long issued = 0;
@@ -568,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_kernel(const __grid_constant
         }
         return;
     }
-    consumers<MAXNP>(a, ring, xs, red, red_norm, full, empty, s_abort);
+    consumers<MAXNP, COMBINE>(a, ring, xs, red, red_norm, full, empty, cfull, cempty, geom, s_abort);
 }
 
 // The two bounded waits of the step kernel run alone, each on something that
@@ -603,15 +684,17 @@ cudaError_t launch_wait_probe(unsigned* sync, int* status, int which, uint32_t l
 }
 
 int step_smem_bytes(int rows) {
-    return 1024 + ring_depth(rows) * kStage + xs_bytes(rows) + kRedBytes + 8 * kStepMaxRows * 4 + 2 * kMaxDepth * 8 + 64;
+    return 1024 + ring_depth(rows) * kStage + xs_bytes(rows) + kRedBytes + 8 * kStepMaxRows * 4 + 2 * kMaxDepth * 8 +
+           2 * 8 + 16 + 64;
 }
 
 cudaError_t init_step_persistent() {
-    cudaError_t e = cudaFuncSetAttribute(step_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         std::max(step_smem_bytes(1), step_smem_bytes(2)));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(step_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                std::max(step_smem_bytes(1), step_smem_bytes(2)));
+    const int smem = std::max(step_smem_bytes(1), step_smem_bytes(2));
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(step_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
+    if ((e = cudaFuncSetAttribute(step_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
+    if ((e = cudaFuncSetAttribute(step_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem))) return e;
+    return cudaFuncSetAttribute(step_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
 cudaError_t launch_step_persistent(const StepArgs& a, int grid, cudaStream_t st) {
@@ -623,15 +706,28 @@ cudaError_t launch_step_persistent(const StepArgs& a, int grid, cudaStream_t st)
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    // attention units of the step (as attn_blocks x n_kv x attn_groups)
+    int max_pos = 0, groups = 0;
+    for (int s = 0; s < a.rows.n_streams; ++s) {
+        const int rows = a.rows.row_start[s + 1] - a.rows.row_start[s];
+        max_pos = std::max(max_pos, a.rows.pos0[s] + rows - 1);
+        groups += (rows + attn::kGroupRows - 1) / attn::kGroupRows;
+    }
+    const long long units = (long long)(max_pos / kAttnUnit + 1) * a.n_kv * groups;
+    const bool combine = units > grid;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(step_threads(combine));
     cfg.dynamicSmemBytes = step_smem_bytes(a.rows.n_rows);
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     const bool one_row_streams = a.rows.n_rows == a.rows.n_streams;
-    return one_row_streams ? cudaLaunchKernelEx(&cfg, step_kernel<1>, a) : cudaLaunchKernelEx(&cfg, step_kernel<2>, a);
+    if (combine)
+        return one_row_streams ? cudaLaunchKernelEx(&cfg, step_kernel<1, true>, a)
+                               : cudaLaunchKernelEx(&cfg, step_kernel<2, true>, a);
+    return one_row_streams ? cudaLaunchKernelEx(&cfg, step_kernel<1, false>, a)
+                           : cudaLaunchKernelEx(&cfg, step_kernel<2, false>, a);
 }
 
 }  // namespace tfl

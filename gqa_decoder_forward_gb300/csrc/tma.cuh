@@ -71,6 +71,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     return false;
 }
 
+// The same wait that also gives up at once when *abort is raised (a wait
+// between warps of one CTA whose partner may have stopped).
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                   int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < kMbarSpinLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0u) {
+            if (*abort) return false;
+            if (global_ns() - t0 > kMbarWaitNs) break;
+        }
+    }
+    atomicOr(status, kStatusDevice);
+    *abort = 1;
+    return false;
+}
+
 // After an abort: waits, bounded, for the copies of the last `issued` (at
 // most depth) stages a producer armed on a ring of `depth` stages whose next
 // stage is (stage, phase), so that no copy lands in shared memory after the

@@ -96,13 +96,15 @@ def test_33b_decode_window_16_rows_at_20k(orc, long33):
 
 
 @pytest.mark.parametrize("R", [1, 2])
-def test_33b_persistent_step_equals_per_launch_at_131k(long33, R):
+@pytest.mark.parametrize("pos0", [131000, 10000])
+def test_33b_persistent_step_equals_per_launch_at_131k(long33, R, pos0):
     """The persistent decode step (the benchmark's launch configuration) and the
     launch per operation give the same logits, keys and values at 131,000
     positions, so the oracle gate of the per-operation attention above carries
-    over to the persistent step."""
+    over to the persistent step.  Both positions give more attention units than
+    CTAs (the step variant whose combine warps fold all but each CTA's last
+    unit); at 10,000 most CTAs run one unit and a few two."""
     m, kv, _, _ = long33
-    pos0 = 131000
     ids = synth.uniform_ids(63, R, L1.vocab, "cuda")
     k0, v0 = kv.read(0, pos0, R)       # the seeded rows the steps overwrite
     outs = []
