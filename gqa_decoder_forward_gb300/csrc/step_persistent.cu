@@ -226,7 +226,7 @@ struct RingPos {
     }
 };
 
-// ---- producer (warp 8, lane 0) ------------------------------------------------
+// ---- producer (the last warp, lane 0) -------------------------------------------
 // Fills the ring in exactly the order the consumers drain it.
 // rp / issued: the next ring stage and the number of stages armed so far
 // (read by the caller to drain the ring after an abort).
